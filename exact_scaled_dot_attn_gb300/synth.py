@@ -1,0 +1,103 @@
+"""Seeded synthetic workloads: shapes, seeds and input draws.
+
+This module holds no attention arithmetic. It only draws the fp16 inputs and
+the key lengths that both the CUDA path and the CPU oracle are fed, so the two
+sides see identical bits.
+
+Recipe (one numpy PCG64 stream per workload, seeded with the workload's seed):
+  Q ~ N(0, sigma_qk^2), then K ~ N(0, sigma_qk^2), then V ~ N(0, sigma_v^2),
+  each drawn as float32 standard normals times sigma and rounded to fp16
+  (round-to-nearest-even), shape [B, H, N, d]; then, for padded workloads,
+  key_lengths[b] ~ uniform integer in [lo, hi] (inclusive).
+
+The shapes are the workloads the method is measured on: a tiny exact check, a
+cross-encoder reranking batch (the "cuda-reranker" README's shape class: many
+short padded sequences at head dimension 32), an LLM prefill, a long-context
+prefill whose naive score matrix would not fit ("Naive Attention Kernel",
+section "The Memory Problem"), and a numerics stress case with peaked rows.
+No public dataset is used; these synthetic draws stand in for the reranker's
+retrieval corpus.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    sigma_qk: float = 1.0
+    sigma_v: float = 1.0
+    key_len_range: tuple[int, int] | None = None  # inclusive [lo, hi] when padded
+    check_lse: bool = False
+    ignore_padded_queries: bool = False
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def describe(self) -> str:
+        mask = "causal" if self.causal else "no mask"
+        if self.key_len_range:
+            mask = f"key padding L~U[{self.key_len_range[0]},{self.key_len_range[1]}]"
+        return f"{self.name} B={self.B} H={self.H} N={self.N} d={self.d} {mask}"
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 2, 128, 64, False, seed=1),
+    "rerank": Workload("rerank", 50, 12, 256, 32, False, seed=2, key_len_range=(64, 256),
+                       ignore_padded_queries=True),
+    "prefill": Workload("prefill", 4, 32, 4096, 128, True, seed=3),
+    "long": Workload("long", 1, 32, 32768, 128, True, seed=4),
+    "stress": Workload("stress", 2, 16, 8192, 64, False, seed=5, sigma_qk=3.0, check_lse=True),
+}
+
+
+def draw(B: int, H: int, N: int, d: int, seed: int, *, sigma_qk: float = 1.0,
+         sigma_v: float = 1.0, key_len_range: tuple[int, int] | None = None):
+    """Returns (q, k, v, key_lengths): fp16 arrays [B,H,N,d] and int32 [B] or None."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shape = (B, H, N, d)
+
+    def normal(sigma):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        if sigma != 1.0:
+            x *= np.float32(sigma)
+        return x.astype(np.float16)
+
+    q = normal(sigma_qk)
+    k = normal(sigma_qk)
+    v = normal(sigma_v)
+    kl = None
+    if key_len_range is not None:
+        lo, hi = key_len_range
+        kl = rng.integers(lo, hi + 1, size=B, dtype=np.int64).astype(np.int32)
+    return q, k, v, kl
+
+
+def draw_workload(w: Workload):
+    return draw(w.B, w.H, w.N, w.d, w.seed, sigma_qk=w.sigma_qk, sigma_v=w.sigma_v,
+                key_len_range=w.key_len_range)
+
+
+def attention_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
+    """Contract FLOP count: 4*B*H*N^2*d (2d for QK^T and 2d for PV per pair), halved when causal."""
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def min_bytes(B: int, H: int, N: int, d: int, lse: bool = False) -> int:
+    """Minimum HBM traffic: Q, K, V read once and O written once (fp16), plus fp32 lse."""
+    b = 4 * B * H * N * d * 2
+    if lse:
+        b += 4 * B * H * N
+    return b

@@ -1,0 +1,117 @@
+"""fp64 CPU oracle for exact scaled dot-product attention (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package. It shares no code with the CUDA library: the
+arithmetic lives in ``attn_oracle.c`` (plain C, fp64), and this module only
+compiles it with gcc and marshals numpy arrays into it.
+
+What it computes is stated in the header of ``attn_oracle.c``: the plain
+definition O = softmax(scale * Q K^T + mask) V row by row, with the two-pass
+(max, normaliser, divide) softmax of "Tensor Parallelism with CUDA - Standard
+Attention", section "Step 2: Softmax", and the logsumexp of each row.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "libattn_oracle.so")
+_default = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle source into a shared library (skipped when up to date)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """ctypes handle on one compiled copy of the oracle."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        lib.oracle_half_to_double.restype = ctypes.c_double
+        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_attn.restype = ctypes.c_int
+        lib.oracle_attn.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ]
+        self._lib = lib
+
+    def half_to_double(self, bits: int) -> float:
+        """Decode one binary16 bit pattern with the oracle's own decoder."""
+        return self._lib.oracle_half_to_double(bits)
+
+    def attn(self, q, k, v, *, sm_scale: float, causal: bool = False, key_lengths=None,
+             rows=None, threads: int | None = None):
+        """Oracle forward.
+
+        q, k, v: numpy float16 arrays of shape [B, H, N, d].
+        key_lengths: int array [B] or None. rows: ascending flat row ids
+        ((b*H + h)*N + i) or None for every row.
+        Returns (o, lse) as float64: o is [B,H,N,d] (or [len(rows), d]), lse is
+        [B,H,N] (or [len(rows)]).
+        """
+        q = np.ascontiguousarray(q, dtype=np.float16)
+        k = np.ascontiguousarray(k, dtype=np.float16)
+        v = np.ascontiguousarray(v, dtype=np.float16)
+        if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        B, H, N, d = q.shape
+        kl = None
+        if key_lengths is not None:
+            kl = np.ascontiguousarray(key_lengths, dtype=np.int32)
+            if kl.shape != (B,):
+                raise ValueError("key_lengths must have shape [B]")
+        if rows is None:
+            n_rows = B * H * N
+            o = np.empty((B, H, N, d), np.float64)
+            lse = np.empty((B, H, N), np.float64)
+            rows_arr = None
+        else:
+            rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+            n_rows = rows_arr.size
+            o = np.empty((n_rows, d), np.float64)
+            lse = np.empty((n_rows,), np.float64)
+        rc = self._lib.oracle_attn(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, N, d, float(sm_scale),
+            int(bool(causal)), None if kl is None else kl.ctypes.data,
+            None if rows_arr is None else rows_arr.ctypes.data, n_rows,
+            o.ctypes.data, lse.ctypes.data, int(threads or default_threads()))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attn failed with code {rc}")
+        return o, lse
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def half_to_double(bits: int) -> float:
+    return default().half_to_double(bits)
+
+
+def attn(q, k, v, **kw):
+    """Oracle forward with the default build; see ``Oracle.attn``."""
+    return default().attn(q, k, v, **kw)

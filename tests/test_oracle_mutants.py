@@ -1,0 +1,43 @@
+"""Plant plausible mistakes in copies of the oracle (CPU only) and check that the pins catch
+each one: a dropped term, a wrong sign, an off-by-one mask, a swapped operand, a missing
+normalisation. The real oracle source is never modified; each mutant is a patched copy
+compiled into a temporary directory."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTANTS = {
+    "dropped_scale": ("s[j] = sm_scale * dot;", "s[j] = dot;"),
+    "causal_off_by_one": ("if (causal && j > i)", "if (causal && j >= i)"),
+    "padding_off_by_one": ("if (j >= L)", "if (j > L)"),
+    "lse_dropped_max": ("*lse = m + log(l);", "*lse = log(l);"),
+    "no_normalisation": ("double p = exp(s[j] - m) / l;", "double p = exp(s[j] - m);"),
+    "wrong_sign_exponent": ("double p = exp(s[j] - m) / l;", "double p = exp(m - s[j]) / l;"),
+    "v_uses_k": ("o[c] += p * V[j * d + c];", "o[c] += p * K[j * d + c];"),
+    "q_dot_v": ("dot += q[c] * K[j * d + c];", "dot += q[c] * V[j * d + c];"),
+    "normaliser_without_mask": ("if (allowed(i, j, L, causal))\n            l += exp(s[j] - m);",
+                                "if (1)\n            l += exp(s[j] - m);"),
+    "decoder_bias": ("mag = ldexp((double)(1024 + f), e - 25);", "mag = ldexp((double)(1024 + f), e - 24);"),
+    "subnormal_scale": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")).read()
+    assert src.count(before) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / f"mutant_{name}.c"
+    mutated.write_text(src.replace(before, after))
+    lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / f"libmutant_{name}.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except Exception:  # an assertion, or an error the broken arithmetic provokes
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutant {name}"
