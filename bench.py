@@ -1,0 +1,385 @@
+"""Benchmark of the attention forward on GB300: one JSON line on stdout (rank 0).
+
+Default workload: LLM prefill, B=4, H=32, N=4096, d=128, causal, fp16 (the headline
+metric: attention-forward TFLOP/s against the dense fp16 tensor peak). A step is one
+forward over the whole batch with inputs resident in HBM. The same line carries:
+  e2e          the same metric through the public API with host tensors (pinned host ->
+               device copies of Q, K, V and the device -> host copy of O inside the timing)
+  short_n      the reranking workload (B=50, H=12, N=256, d=32, key padding) in GB/s of
+               minimum traffic, L2 flushed before every timed launch
+  roofline     the dominant kernel's achieved FLOP/s against the measured peak
+  cpu_baseline the fp64 oracle timed on the host cores on a bounded sample (rank 0, N=1)
+  clocks       SM clocks and throttle reasons sampled during the timed region
+
+--impl reference times the oracle itself (the reference arm: a CPU program) on the same
+workload, metric and unit.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own copy of the workload
+(independent (batch, head) problems, no collective on the data path); the time is the
+max over ranks and the value counts the work of all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_scaled_dot_attn_gb300 import synth  # noqa: E402
+
+METRIC = "attn fwd TFLOPS & % of GB300 fp16 dense peak (N=4096,d=128,causal); GB/s short-N"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-short-n", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling (every 200 ms) of SM clocks and throttle reasons."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1] and parts[1] not in self.uuid:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU arm
+def oracle_sample(w, q, k, v, kl, heads):
+    """Times the oracle on every row of the given heads of batch 0; returns (flops, s, cores)."""
+    import numpy as np
+
+    import oracle
+    rows = np.concatenate([np.arange(h * w.N, (h + 1) * w.N) for h in heads]).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal, key_lengths=kl, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = synth.attention_flops(1, len(heads), w.N, w.d, w.causal)
+    return flops, dt, oracle.default_threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    q, k, v, kl = synth.draw_workload(w)
+    oracle.build()
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+    # Each step: every row of one (batch 0) head, sized so the whole run stays within minutes.
+    n_heads = 1
+    per_step = []
+    for s in range(warmup + steps):
+        h = s % w.H
+        flops, dt, cores = oracle_sample(w, q, k, v, kl, [h])
+        if s >= warmup:
+            per_step.append((flops, dt))
+        if s >= warmup + 1 and sum(t for _, t in per_step) > 120:
+            break  # the oracle is slow by design; keep the arm bounded
+    total_f = sum(f for f, _ in per_step)
+    total_t = sum(t for _, t in per_step)
+    value = total_f / total_t / 1e12
+    sample = (f"{len(per_step)} steps x {n_heads} head(s) of batch 0, all {w.N} rows each "
+              f"({w.describe()})")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": len(per_step), "warmup": warmup, "ms_per_step": total_t / len(per_step) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "causal": w.causal, "sm_scale": w.sm_scale,
+            "key_lengths": list(w.key_len_range) if w.key_len_range else None,
+            "l2": "inputs larger than L2" if synth.min_bytes(w.B, w.H, w.N, w.d) > 2 * 129e6
+            else "L2 flushed between timed launches"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def traffic_from_profile(kernel_name: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_name}_{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            key, val = line.split(":", 1)
+            vals[key.strip()] = val.strip()
+    src = vals.get("source_file")
+    if not src or not os.path.exists(os.path.join(ROOT, src)):
+        return None
+    digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+    if digest != vals.get("source_sha256_16"):
+        return None  # the kernel changed since the counters were taken
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def l2_flush_buffer(torch):
+    return torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+
+
+def time_launches(torch, fn, n, flush=None):
+    """Per-launch CUDA-event durations (ms) on the current stream."""
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush.fill_(1)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from exact_scaled_dot_attn_gb300 import api, build
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    build.build()
+    peaks, peak_src = load_peaks()
+    w = synth.WORKLOADS[args.workload]
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+
+    q, k, v, kl = synth.draw_workload(w)
+    qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    kld = torch.from_numpy(kl).cuda() if kl is not None else None
+    od = torch.empty_like(qd)
+    flops = synth.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+
+    def step():
+        api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od,
+                path=args.path)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading under load
+    for _ in range(max(3, warmup)):
+        step()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    region_ms = evs[0][0].elapsed_time(evs[-1][1])
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        t = torch.tensor([region_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        region_ms = float(t.item())
+    ms_per_step = region_ms / steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # End to end through the public API with host tensors.
+    e2e_steps = max(1, min(args.e2e_steps, steps))
+    tq, tk, tv = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+    tkl = torch.from_numpy(kl) if kl is not None else None
+    o_host = torch.empty(q.shape, dtype=torch.float16, pin_memory=True)
+    for _ in range(2):
+        api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
+                path=args.path)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
+                path=args.path)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(x.nbytes for x in (q, k, v)) + (kl.nbytes if kl is not None else 0)
+    d2h = q.nbytes
+
+    # Roofline of the dominant (only) kernel.
+    kernel_name = api.auto_path(w.N, w.d) if args.path == "auto" else args.path
+    avg_launch_ms = statistics.mean(launch_ms)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_from_profile(kernel_name, w.name),
+                "kernel": kernel_name, "peak_source": f"{peak_src} bf16 dense burst (fp16 rate = bf16 rate)",
+                "avg_launch_ms": avg_launch_ms}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": dict(workload_config(w), path=args.path, kernel=kernel_name),
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": steps,
+        "roofline": roofline,
+        "clocks": clocks,
+    }
+
+    if not args.no_short_n:
+        line["short_n"] = short_n(torch, api, peaks, peak_src)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_heads = 2
+        f, dt, cores = oracle_sample(w, q, k, v, kl, list(range(n_heads)))
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"batch 0, heads 0..{n_heads - 1}, all {w.N} rows "
+                                          f"({n_heads}/{w.B * w.H} of the workload), {dt:.1f} s"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def short_n(torch, api, peaks, peak_src):
+    """Reranking workload in GB/s of minimum traffic, L2 flushed before each timed launch."""
+    w = synth.WORKLOADS["rerank"]
+    q, k, v, kl = synth.draw_workload(w)
+    qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    kld = torch.from_numpy(kl).cuda()
+    od = torch.empty_like(qd)
+
+    def fn():
+        api.fwd(qd, kd, vd, causal=False, sm_scale=w.sm_scale, key_lengths=kld, out=od)
+
+    flush = l2_flush_buffer(torch)
+    time_launches(torch, fn, 5, flush)
+    ms = time_launches(torch, fn, 50, flush)
+    med = statistics.median(ms)
+    nbytes = synth.min_bytes(w.B, w.H, w.N, w.d) + kl.nbytes
+    gbs = nbytes / (med * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    valid_bytes = int(sum(int(L) for L in kl) * w.H * w.d * 2 * 2 + q.nbytes * 2)
+    return {"workload": w.describe(), "value": gbs, "unit": "GB/s", "median_launch_ms": med,
+            "bytes": nbytes, "valid_only_bytes": valid_bytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_source": f"{peak_src} copy bandwidth"},
+            "l2": "flushed (512 MiB write) before every timed launch"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

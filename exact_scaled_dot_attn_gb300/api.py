@@ -1,0 +1,114 @@
+"""Python entry point over the C ABI: ``fwd(q, k, v, ...)``.
+
+PyTorch supplies device memory and the current CUDA stream; every step of the
+attention runs in the CUDA library. Host (CPU) tensors are accepted too: they
+are copied to the current device, the same C entry point runs on them, and the
+results are copied back (this is the end-to-end call a host-side user makes).
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+
+def _check_device_tensor(name, t, shape, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+        sm_scale: float | None = None, key_lengths: torch.Tensor | None = None,
+        return_lse: bool = False, out: torch.Tensor | None = None,
+        lse_out: torch.Tensor | None = None, path: str = "auto"):
+    """O = softmax(sm_scale * Q K^T + mask) V for fp16 [B, H, N, d] tensors.
+
+    causal: key j allowed for query i only when j <= i.
+    key_lengths: int32 [B]; keys j >= key_lengths[b] are excluded.
+    sm_scale: defaults to 1/sqrt(d).
+    return_lse: also return the fp32 [B, H, N] logsumexp.
+    path: "auto", "warp_mma" or "tcgen05" (kernel choice; see include/attn.h).
+    Device tensors run asynchronously on the current stream. CPU tensors are
+    copied to the current CUDA device and back, and the call returns after the
+    copy back has finished.
+    """
+    if q.device.type == "cpu":
+        return _fwd_host(q, k, v, causal=causal, sm_scale=sm_scale, key_lengths=key_lengths,
+                         return_lse=return_lse, out=out, lse_out=lse_out, path=path)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_device_tensor(name, t, (B, H, N, d), torch.float16, dev)
+    if dev.type != "cuda":
+        raise ValueError("tensors must be CUDA tensors (or CPU tensors for the host path)")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_device_tensor("out", out, (B, H, N, d), torch.float16, dev)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, H, N), device=dev,
+                                                               dtype=torch.float32)
+        _check_device_tensor("lse_out", lse, (B, H, N), torch.float32, dev)
+    if key_lengths is not None:
+        _check_device_tensor("key_lengths", key_lengths, (B,), torch.int32, dev)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    if path not in _lib.PATHS:
+        raise ValueError(f"path must be one of {sorted(_lib.PATHS)}")
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = _lib.lib().attn_fwd_path(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, B, H, N, d, float(sm_scale),
+            int(bool(causal)), key_lengths.data_ptr() if key_lengths is not None else None,
+            _lib.PATHS[path], stream)
+    if st != _lib.ATTN_OK:
+        raise _lib.AttnError(st, "attn_fwd_path")
+    return (out, lse) if return_lse else out
+
+
+def _fwd_host(q, k, v, *, causal, sm_scale, key_lengths, return_lse, out, lse_out, path):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    qd = q.to(dev, non_blocking=True)
+    kd = k.to(dev, non_blocking=True)
+    vd = v.to(dev, non_blocking=True)
+    kld = key_lengths.to(dev, non_blocking=True) if key_lengths is not None else None
+    res = fwd(qd, kd, vd, causal=causal, sm_scale=sm_scale, key_lengths=kld,
+              return_lse=return_lse, path=path)
+    o_dev, lse_dev = res if return_lse else (res, None)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float16, pin_memory=True)
+    out.copy_(o_dev, non_blocking=True)
+    if return_lse:
+        if lse_out is None:
+            lse_out = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
+        lse_out.copy_(lse_dev, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return (out, lse_out) if return_lse else out
+
+
+def auto_path(N: int, d: int) -> str:
+    """Name of the kernel the "auto" path runs for sequence length N and head dimension d."""
+    code = _lib.lib().attn_auto_path(int(N), int(d))
+    for name, c in _lib.PATHS.items():
+        if c == code and name != "auto":
+            return name
+    raise ValueError(f"unsupported head dimension {d}")
+
+
+def read_device_status() -> int:
+    """Synchronizes the current stream and returns (and clears) the device status word."""
+    stream = torch.cuda.current_stream().cuda_stream
+    return _lib.lib().attn_read_device_status(stream)

@@ -1,0 +1,164 @@
+// C-ABI front end: argument validation, kernel choice and launch.
+// The operation and the contract of every entry point are stated in include/attn.h.
+#include "attn.h"
+#include "attn_internal.h"
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace {
+
+// Per-device status word written by kernels whose bounded waits run out.
+__device__ unsigned int g_attn_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+unsigned int *g_status_ptr[kMaxDevices];
+
+// Device address of the status word for the current device (looked up once per device).
+cudaError_t status_word(unsigned int **out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_attn_device_status);
+        if (err != cudaSuccess)
+            return err;
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+attn_status_t validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                       int B, int H, int N, int d, float sm_scale, int causal,
+                       const int32_t *key_lengths)
+{
+    if (!q || !k || !v || !o)
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1)
+        return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1)
+        return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale))
+        return ATTN_ERR_INVALID_ARG;
+    if (d != 32 && d != 64 && d != 128)
+        return ATTN_ERR_UNSUPPORTED;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    if (bh > INT32_MAX)
+        return ATTN_ERR_INVALID_ARG;
+    if (bh * N > INT64_MAX / d) // element count of one tensor must fit int64
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return ATTN_ERR_MISALIGNED;
+    if ((lse && !aligned(lse, 4)) || (key_lengths && !aligned(key_lengths, 4)))
+        return ATTN_ERR_MISALIGNED;
+    return ATTN_OK;
+}
+
+} // namespace
+
+extern "C" const char *attn_status_str(attn_status_t status)
+{
+    switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension or path";
+    case ATTN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "bounded on-chip wait ran out";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int attn_auto_path(int N, int d)
+{
+    if (d != 32 && d != 64 && d != 128)
+        return -1;
+    (void)N;
+    return ATTN_PATH_WARP_MMA;
+}
+
+extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,
+                                       float *lse, int B, int H, int N, int d, float sm_scale,
+                                       int causal, const int32_t *key_lengths, int path,
+                                       attn_stream_t stream)
+{
+    attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
+    if (st != ATTN_OK)
+        return st;
+    if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05)
+        return ATTN_ERR_UNSUPPORTED;
+    if (path == ATTN_PATH_TCGEN05 && d == 32)
+        return ATTN_ERR_UNSUPPORTED;
+    if (path == ATTN_PATH_AUTO)
+        path = attn_auto_path(N, d);
+
+    attn::FwdParams p;
+    p.q = static_cast<const __half *>(q);
+    p.k = static_cast<const __half *>(k);
+    p.v = static_cast<const __half *>(v);
+    p.o = static_cast<__half *>(o);
+    p.lse = lse;
+    p.key_lengths = key_lengths;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = d;
+    p.sm_scale = sm_scale;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.causal = causal;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (path == ATTN_PATH_TCGEN05) {
+        unsigned int *status = nullptr;
+        err = status_word(&status);
+        if (err == cudaSuccess)
+            err = attn::launch_tcgen05(p, s, status);
+    } else {
+        err = attn::launch_warp_mma(p, s);
+    }
+    return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" attn_status_t attn_fwd_lse(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int B, int H, int N, int d, float sm_scale,
+                                      int causal, const int32_t *key_lengths, attn_stream_t stream)
+{
+    return attn_fwd_path(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths,
+                         ATTN_PATH_AUTO, stream);
+}
+
+extern "C" attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, int B,
+                                  int H, int N, int d, float sm_scale, int causal,
+                                  const int32_t *key_lengths, attn_stream_t stream)
+{
+    return attn_fwd_path(q, k, v, o, nullptr, B, H, N, d, sm_scale, causal, key_lengths,
+                         ATTN_PATH_AUTO, stream);
+}
+
+extern "C" attn_status_t attn_read_device_status(attn_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    unsigned int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_attn_device_status, sizeof(value)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (value != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_attn_device_status, &zero, sizeof(zero)) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        return ATTN_ERR_TIMEOUT;
+    }
+    return ATTN_OK;
+}

@@ -1,0 +1,32 @@
+// Internal interface between the C-ABI front end (attn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct FwdParams {
+    const __half *q;
+    const __half *k;
+    const __half *v;
+    __half *o;
+    float *lse;                 // may be null
+    const int32_t *key_lengths; // may be null
+    int B, H, N, d;
+    float sm_scale;
+    float scale_log2; // sm_scale * log2(e): scores are exponentiated with exp2
+    int causal;
+};
+
+// Warp-level mma.sync kernel (every d in {32, 64, 128}, every N).
+cudaError_t launch_warp_mma(const FwdParams &p, cudaStream_t stream);
+
+// TMA + tcgen05/TMEM kernel (d in {64, 128}). `status` is the device status word.
+cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status);
+
+// Status codes the kernels write into the device status word.
+constexpr unsigned int kDevStatusTimeout = 1u;
+
+} // namespace attn

@@ -1,0 +1,113 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact scaled dot-product attention forward.
+ *
+ * The operation, for every batch b, head h and query row i of a self-attention
+ * problem with N queries and N keys per head:
+ *
+ *     O_i = sum_j softmax_j( sm_scale * q_i . k_j + mask_ij ) v_j
+ *
+ * ("Tensor Parallelism with CUDA - Standard Attention", sections "Step 1: QK^T",
+ * "Step 2: Softmax" and "Step 3: PV"; the additive mask of "Naive Attention
+ * Kernel", section "1. Standard Attention: Step by Step", restricted to the two
+ * structured masks below). The kernels follow the tiled recurrence of
+ * "Self-Attention Kernel & Inference Engine from Scratch", sections "Online
+ * Softmax Formulation" and "CUDA Kernel Structure": Q, K and V tiles are staged
+ * on chip and the N x N score matrix is never written to memory.
+ *
+ * Masks (mask_ij is 0 or -inf):
+ *   causal        key j is allowed for query i only when j <= i (square, top-left aligned);
+ *   key_lengths   key j of batch b is allowed only when j < clamp(key_lengths[b], 0, N)
+ *                 (the key-padding mask of the "cuda-reranker" README). Padded query rows
+ *                 (i >= key_lengths[b]) are computed like any other row.
+ *   A row whose allowed set is empty gets O_i = 0 and lse_i = -inf.
+ *
+ * Data layout and types (all tensors contiguous, d innermost):
+ *   q, k, v   fp16 (IEEE binary16) [B, H, N, d], device memory
+ *   o         fp16 [B, H, N, d], device memory, written (rounded to nearest even)
+ *   lse       fp32 [B, H, N] natural-log logsumexp of the scaled allowed scores, or NULL
+ *   key_lengths  int32 [B] in device memory, or NULL (= N for every batch)
+ * Arithmetic: fp16 products, fp32 accumulation, fp32 row statistics; the
+ * probabilities are rounded to fp16 before the PV product.
+ *
+ * Ownership: the caller owns every buffer. The entry points allocate no memory,
+ * keep no per-call state and are safe to call from several host threads.
+ *
+ * Errors: argument errors are returned synchronously, before anything is
+ * launched. Launch failures return ATTN_ERR_CUDA. The work is asynchronous on
+ * `stream` (NULL = the legacy default stream) and the call does not
+ * synchronize; device-side faults surface at the caller's next synchronizing
+ * CUDA call. Kernels that wait on on-chip barriers bound every wait; a wait that
+ * runs out ends the block early and records ATTN_ERR_TIMEOUT in a per-device
+ * status word that attn_read_device_status() returns.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* NULL tensor pointer, B/H/N < 1, non-finite sm_scale, size overflow */
+    ATTN_ERR_UNSUPPORTED = 2, /* head dimension other than 32, 64 or 128; unknown path */
+    ATTN_ERR_MISALIGNED = 3,  /* a tensor pointer that is not 16-byte aligned */
+    ATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+    ATTN_ERR_TIMEOUT = 5      /* a bounded on-chip wait ran out (see attn_read_device_status) */
+} attn_status_t;
+
+/* Which kernel runs the forward. AUTO picks by shape: the tcgen05 kernel for
+ * d in {64, 128} with N > 256, the warp-level kernel otherwise. */
+typedef enum {
+    ATTN_PATH_AUTO = 0,
+    ATTN_PATH_WARP_MMA = 1, /* warp-level mma.sync tile kernel: every d, every N */
+    ATTN_PATH_TCGEN05 = 2   /* TMA + tcgen05/TMEM warp-specialised kernel: d in {64, 128} */
+} attn_path_t;
+
+/*
+ * Forward without logsumexp. Arguments as described above:
+ *   q, k, v, o   device pointers, 16-byte aligned, fp16 [B,H,N,d]
+ *   B, H, N      >= 1; B*H*N*d must fit in int64 and B*H in int32
+ *   d            32, 64 or 128 (the head dimensions of the "CUDA Kernel Structure" template)
+ *   sm_scale     finite; 1/sqrt(d) is the usual choice ("Why Divide by sqrt(d)?")
+ *   causal       0 or 1
+ *   key_lengths  device int32 [B] or NULL
+ *   stream       CUDA stream or NULL
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, int B, int H, int N,
+                       int d, float sm_scale, int causal, const int32_t *key_lengths,
+                       attn_stream_t stream);
+
+/* Forward that also writes lse (fp32 [B,H,N], device, 4-byte aligned) when lse != NULL. */
+attn_status_t attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                           int H, int N, int d, float sm_scale, int causal,
+                           const int32_t *key_lengths, attn_stream_t stream);
+
+/* attn_fwd_lse with an explicit kernel choice (attn_path_t). ATTN_PATH_TCGEN05 with
+ * d = 32 returns ATTN_ERR_UNSUPPORTED. Used to check each kernel on every shape. */
+attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int N, int d, float sm_scale, int causal,
+                            const int32_t *key_lengths, int path, attn_stream_t stream);
+
+/* The kernel ATTN_PATH_AUTO selects for sequence length N and head dimension d
+ * (an attn_path_t value), or -1 when d is unsupported. No CUDA call is made. */
+int attn_auto_path(int N, int d);
+
+/* Static description of a status code. Never NULL. */
+const char *attn_status_str(attn_status_t status);
+
+/* Synchronizes `stream`, then reads and clears the device-side status word of
+ * the current device: ATTN_OK, or ATTN_ERR_TIMEOUT when a bounded wait in an
+ * earlier launch ran out. ATTN_ERR_CUDA if the synchronization fails. */
+attn_status_t attn_read_device_status(attn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

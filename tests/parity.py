@@ -1,0 +1,121 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C ABI and compare
+with the fp64 oracle element by element.
+
+Tolerances (fp16 inputs and output, fp16 probabilities, fp32 accumulation):
+  max |O_gpu - O_ref|           <= 1e-2
+  ||O_gpu - O_ref||_2 / ||O_ref||_2 <= 2e-3
+  max |lse_gpu - lse_ref|       <= 1e-3   (finite rows; empty rows must be -inf on both sides)
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from exact_scaled_dot_attn_gb300 import _lib, api, build
+
+TOL_MAX_ABS = 1e-2
+TOL_REL_L2 = 2e-3
+TOL_LSE = 1e-3
+
+_built = False
+
+
+def ensure_built():
+    global _built
+    if not _built:
+        build.build()
+        _built = True
+
+
+def to_dev(x):
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def run_gpu(q, k, v, *, causal, key_lengths=None, sm_scale=None, path="auto", guard=True):
+    """Runs the C-ABI forward on device copies of the numpy inputs.
+
+    O and lse are allocated inside larger buffers whose margins hold a sentinel, and the
+    interior is pre-filled with NaN, so writes out of bounds and rows left unwritten both
+    show up. Returns numpy (o, lse) as float64.
+    """
+    ensure_built()
+    B, H, N, d = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(d)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    kld = to_dev(key_lengths)
+    pad_o = 4096  # fp16 elements of guard on each side (8 KiB: keeps 16-byte alignment)
+    pad_l = 1024
+    n_o = q.size
+    n_l = B * H * N
+    o_buf = torch.full((n_o + 2 * pad_o,), float("nan"), dtype=torch.float16, device="cuda")
+    l_buf = torch.full((n_l + 2 * pad_l,), float("nan"), dtype=torch.float32, device="cuda")
+    o_buf[:pad_o] = 1234.0
+    o_buf[pad_o + n_o:] = 1234.0
+    l_buf[:pad_l] = 4321.0
+    l_buf[pad_l + n_l:] = 4321.0
+    o = o_buf[pad_o:pad_o + n_o].view(B, H, N, d)
+    lse = l_buf[pad_l:pad_l + n_l].view(B, H, N)
+    api.fwd(qd, kd, vd, causal=causal, sm_scale=sm_scale, key_lengths=kld, return_lse=True,
+            out=o, lse_out=lse, path=path)
+    st = api.read_device_status()
+    assert st == _lib.ATTN_OK, f"device status {st}"
+    torch.cuda.synchronize()
+    if guard:
+        assert torch.all(o_buf[:pad_o] == 1234.0) and torch.all(o_buf[pad_o + n_o:] == 1234.0), \
+            "O guard region overwritten"
+        assert torch.all(l_buf[:pad_l] == 4321.0) and torch.all(l_buf[pad_l + n_l:] == 4321.0), \
+            "lse guard region overwritten"
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, *, row_mask=None, check_lse=True, what=""):
+    """Element-wise comparison; row_mask (bool, per row) selects the rows that count."""
+    o_gpu = o_gpu.reshape(-1, o_gpu.shape[-1])
+    o_ref = o_ref.reshape(-1, o_ref.shape[-1])
+    lse_gpu = lse_gpu.reshape(-1)
+    lse_ref = lse_ref.reshape(-1)
+    if row_mask is not None:
+        row_mask = np.asarray(row_mask).reshape(-1)
+        o_gpu, o_ref = o_gpu[row_mask], o_ref[row_mask]
+        lse_gpu, lse_ref = lse_gpu[row_mask], lse_ref[row_mask]
+    assert not np.isnan(o_gpu).any(), f"{what}: NaN in O (unwritten or invalid rows)"
+    err = np.abs(o_gpu - o_ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    ref_norm = float(np.linalg.norm(o_ref))
+    rel = float(np.linalg.norm(o_gpu - o_ref) / ref_norm) if ref_norm > 0 else float(np.linalg.norm(o_gpu))
+    assert max_abs <= TOL_MAX_ABS, f"{what}: max |dO| = {max_abs:.3e}"
+    assert rel <= TOL_REL_L2, f"{what}: rel L2 = {rel:.3e}"
+    lse_err = 0.0
+    if check_lse:
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(lse_gpu), fin), f"{what}: lse finiteness differs"
+        assert np.all(lse_gpu[~fin] == -np.inf), f"{what}: empty rows must have lse = -inf"
+        if fin.any():
+            lse_err = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max())
+            assert lse_err <= TOL_LSE, f"{what}: max |dlse| = {lse_err:.3e}"
+    return dict(max_abs=max_abs, rel_l2=rel, lse_max_abs=lse_err)
+
+
+def oracle_full(q, k, v, *, causal, key_lengths=None, sm_scale=None):
+    d = q.shape[-1]
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(d)
+    return oracle.attn(q, k, v, sm_scale=sm_scale, causal=causal, key_lengths=key_lengths)
+
+
+def sample_rows(B, H, N, seed, per_head=48, heads=None):
+    """Deterministic sample of flat row ids: tile edges, ragged tail and random rows in a few
+    heads (first, last and random ones)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    BH = B * H
+    if heads is None:
+        heads = sorted({0, BH - 1, *rng.integers(0, BH, size=2).tolist()})
+    rows = []
+    fixed = [0, 1, 63, 64, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    for h in heads:
+        picks = {i for i in fixed if 0 <= i < N}
+        picks |= set(rng.integers(0, N, size=per_head).tolist())
+        rows += [h * N + i for i in sorted(picks)]
+    return np.array(sorted(rows), dtype=np.int64)

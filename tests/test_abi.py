@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads, exports every symbol include/attn.h declares, and rejects
+bad arguments synchronously (CPU only: no call here reaches a CUDA API)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_scaled_dot_attn_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_fwd_lse", "attn_fwd_path", "attn_status_str",
+                     "attn_read_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_exported(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(names) == set(_lib.SIGNATURES), "Python binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code in range(0, 6):
+        s = _lib.status_str(code)
+        assert s and s != "unknown status"
+    assert _lib.status_str(99) == "unknown status"
+
+
+# Fake, never-dereferenced device addresses: validation must reject before any CUDA call.
+A = 0x10000
+
+
+def call(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=8, d=64, scale=0.125, causal=0,
+         kl=None, path=0):
+    return lib.attn_fwd_path(q, k, v, o, lse, B, H, N, d, scale, causal, kl, path, None)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(q=None), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(k=None), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(v=None), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(H=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(N=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=48), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(path=7), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(d=32, path=_lib.PATH_TCGEN05), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(q=A + 8), _lib.ATTN_ERR_MISALIGNED),
+    (dict(o=A + 2), _lib.ATTN_ERR_MISALIGNED),
+    (dict(lse=A + 2), _lib.ATTN_ERR_MISALIGNED),
+    (dict(kl=A + 1), _lib.ATTN_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 16), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(B=1 << 20, H=1 << 10, N=1 << 30, d=128), _lib.ATTN_ERR_INVALID_ARG),
+])
+def test_argument_validation(lib, kw, expected):
+    assert call(lib, **kw) == expected
+
+
+def test_fwd_and_fwd_lse_validate_too(lib):
+    assert lib.attn_fwd(None, A, A, A, 1, 1, 8, 64, 0.1, 0, None, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_lse(A, A, A, A, None, 1, 1, 8, 40, 0.1, 0, None, None) == \
+        _lib.ATTN_ERR_UNSUPPORTED
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.lib()
