@@ -84,8 +84,7 @@ extern "C" int attn_auto_path(int N, int d)
 {
     if (d != 32 && d != 64 && d != 128)
         return -1;
-    (void)N;
-    return ATTN_PATH_WARP_MMA;
+    return (d != 32 && N > 256) ? ATTN_PATH_TCGEN05 : ATTN_PATH_WARP_MMA;
 }
 
 extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,

@@ -1,11 +1,571 @@
-// TMA + tcgen05/TMEM attention forward (d in {64, 128}).
+// TMA + tcgen05/TMEM attention forward for sm_103a (head dimension 64 or 128).
+//
+// The tiled online-softmax recurrence of "Self-Attention Kernel & Inference
+// Engine from Scratch" ("Online Softmax Formulation", "CUDA Kernel Structure"),
+// laid out for the Blackwell tensor core:
+//
+//   work unit   (batch*head, pair of 128-row Q tiles); a persistent grid of one CTA
+//               per SM walks the units heaviest-first in a snake order, so causal
+//               triangles spread evenly without any global counter.
+//   warp 0      TMA producer: Q0/Q1 once per unit, then K_j and V_j through a ring of
+//               shared-memory stages (full/empty mbarriers with transaction counts).
+//               K/V tiles past the causal diagonal or past key_lengths[b] are never
+//               loaded (the block skip of "Engineering Decisions & Trade-offs" and the
+//               padding tile skip of the "cuda-reranker" README).
+//   warp 1      allocates TMEM and issues every tcgen05.mma from one thread:
+//               S_t = Q_t K_j^T (fp16 x fp16 -> fp32 in TMEM) and O_t += P_t V_j with
+//               P_t read from TMEM; completion is signalled with tcgen05.commit.
+//   warps 4-7   softmax warpgroup for Q tile 0, warps 8-11 for Q tile 1: thread r owns
+//               TMEM lane r = query row r. Per K/V tile it reads the S row, scales,
+//               masks, updates the running max m and normaliser l with exp2, and writes
+//               P (fp16) into TMEM over S. The accumulator O is rescaled only when the
+//               row max grows by more than 2^8 over the reference used so far (lazy
+//               correction: O and l always share one reference, so the result is exact).
+//               At the end of the unit it divides O by l, rounds to fp16, stores O and
+//               the logsumexp.
+//
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d); P_t is
+// packed fp16 in the first 64 columns of S_t. Every mbarrier wait is bounded; a wait
+// that runs out sets the abort flag and the device status word and the CTA unwinds.
 #include "attn_internal.h"
+#include "sm100_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <math.h>
+#include <mutex>
 
 namespace attn {
+namespace {
 
-cudaError_t launch_tcgen05(const FwdParams &, cudaStream_t, unsigned int *)
+using namespace sm100;
+
+constexpr int kBM = 128;      // query rows per Q tile
+constexpr int kBN = 128;      // keys per K/V tile
+constexpr int kThreads = 384; // 12 warps
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f; // lazy-correction threshold (log2 units)
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+template <int D> struct Cfg {
+    static constexpr int kBoxBytes = kBM * 128;       // one 128-row x 64-column fp16 TMA box
+    static constexpr int kTileBytes = kBM * D * 2;    // a 128 x D fp16 tile
+    static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring depth
+    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = 2 * kTileBytes;
+    static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffBar + 1024 + 1024; // barriers + alignment slack
+    static constexpr uint32_t kIdescS = idesc_f16_f32(kBM, kBN, 0, 0);
+    static constexpr uint32_t kIdescPV = idesc_f16_f32(kBM, D, 0, 1);
+};
+
+struct TcArgs {
+    FwdParams p;
+    int n_pairs; // ceil(N / 256)
+    int n_units; // n_pairs * B * H
+    unsigned int *status;
+};
+
+struct Unit {
+    int bh, b, q0, L, n_kv;
+    bool q1_valid;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
 {
-    return cudaErrorNotSupported;
+    const int BH = a.p.B * a.p.H;
+    Unit U;
+    const int pair = a.n_pairs - 1 - u / BH; // the last query rows carry the most causal work
+    U.bh = u % BH;
+    U.b = U.bh / a.p.H;
+    U.q0 = pair * 2 * kBM;
+    int L = a.p.N;
+    if (a.p.key_lengths) {
+        L = __ldg(a.p.key_lengths + U.b);
+        L = L < 0 ? 0 : (L > a.p.N ? a.p.N : L);
+    }
+    U.L = L;
+    int kv_end = L;
+    if (a.p.causal)
+        kv_end = min(kv_end, U.q0 + 2 * kBM);
+    U.n_kv = (kv_end + kBN - 1) / kBN;
+    U.q1_valid = U.q0 + kBM < a.p.N;
+    return U;
+}
+
+// Unit of round r for CTA c: consecutive rounds walk the CTAs in opposite directions.
+__device__ __forceinline__ int unit_at(int r, int c, int G)
+{
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+// Barrier block layout (8 bytes each).
+template <int D> struct Bars {
+    static constexpr int kQFull = 0, kQEmpty = 1;
+    static constexpr int kKVFull = 2;
+    static constexpr int kKVEmpty = kKVFull + Cfg<D>::kStages;
+    static constexpr int kSFull = kKVEmpty + Cfg<D>::kStages; // [2]
+    static constexpr int kPFull = kSFull + 2;                 // [2]
+    static constexpr int kOReady = kPFull + 2;                // [2]
+    static constexpr int kOEmpty = kOReady + 2;               // [2]
+    static constexpr int kMmaDone = kOEmpty + 2;
+    static constexpr int kCount = kMmaDone + 1;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tcgen05_kernel(const TcArgs args, const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v)
+{
+    using C = Cfg<D>;
+    using BB = Bars<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    unsigned char *smem = smem_raw + (base - raw_addr);
+    const uint32_t sQ = base + C::kOffQ;
+    const uint32_t sKV = base + C::kOffKV;
+    const uint32_t sBar = base + C::kOffBar;
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * BB::kCount);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const FwdParams &p = args.p;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(BB::kQFull), 1);
+        mbar_init(bar(BB::kQEmpty), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(BB::kKVFull + s), 1);
+            mbar_init(bar(BB::kKVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(BB::kSFull + t), 1);
+            mbar_init(bar(BB::kPFull + t), kBM);
+            mbar_init(bar(BB::kOReady + t), 1);
+            mbar_init(bar(BB::kOEmpty + t), kBM);
+        }
+        mbar_init(bar(BB::kMmaDone), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        *args.status = kDevStatusTimeout;
+    };
+
+    const int G = gridDim.x;
+    const int cta = blockIdx.x;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            uint32_t q_it = 0, kv_it = 0;
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int u = unit_at(r, cta, G);
+                if (u >= args.n_units)
+                    break;
+                const Unit U = decode_unit(args, u);
+                if (U.n_kv == 0)
+                    continue;
+                if (!mbar_wait(bar(BB::kQEmpty), (q_it & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                    fail();
+                    break;
+                }
+                ++q_it;
+                mbar_arrive_expect_tx(bar(BB::kQFull), 2 * C::kTileBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int bx = 0; bx < D / 64; ++bx)
+                        tma_load_3d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &tm_q,
+                                    bar(BB::kQFull), bx * 64, U.q0 + t * kBM, U.bh);
+                for (int j = 0; j < U.n_kv && ok; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t slot = kv_it % C::kStages;
+                        const uint32_t ph = (kv_it / C::kStages) & 1u;
+                        if (!mbar_wait(bar(BB::kKVEmpty + slot), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                            fail();
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(BB::kKVFull + slot), C::kTileBytes);
+                        for (int bx = 0; bx < D / 64; ++bx)
+                            tma_load_3d(sKV + slot * C::kTileBytes + bx * C::kBoxBytes,
+                                        kv == 0 ? &tm_k : &tm_v, bar(BB::kKVFull + slot), bx * 64,
+                                        j * kBN, U.bh);
+                        ++kv_it;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t q_it = 0, kv_it = 0;
+            uint32_t p_it[2] = {0, 0}, oe_it[2] = {0, 0};
+            bool ok = true;
+            auto wait = [&](uint32_t b, uint32_t parity) {
+                if (ok && !mbar_wait(b, parity, abort_flag, kWaitLimitNs)) {
+                    fail();
+                    ok = false;
+                }
+                return ok;
+            };
+            auto issue_s = [&](int t, uint32_t k_slot) {
+                const uint32_t qa = sQ + t * C::kTileBytes;
+                const uint32_t ka = sKV + k_slot * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + (t ? C::kTmemS1 : C::kTmemS0), smem_desc_sw128(qa + off, 16, 1024),
+                           smem_desc_sw128(ka + off, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(BB::kSFull + t));
+            };
+            auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
+                const uint32_t va = sKV + v_slot * C::kTileBytes;
+                const uint32_t s_col = t ? C::kTmemS1 : C::kTmemS0;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tmem + (t ? C::kTmemO1 : C::kTmemO0), tmem + s_col + kk * 8,
+                           smem_desc_sw128(va + kk * 2048, C::kBoxBytes, 1024), C::kIdescPV,
+                           (accumulate || kk > 0) ? 1u : 0u);
+                mma_commit(bar(BB::kOReady + t));
+            };
+            for (int r = 0; ok; ++r) {
+                const int u = unit_at(r, cta, G);
+                if (u >= args.n_units)
+                    break;
+                const Unit U = decode_unit(args, u);
+                if (U.n_kv == 0)
+                    continue;
+                const int nt = U.q1_valid ? 2 : 1;
+                if (!wait(bar(BB::kQFull), q_it & 1u))
+                    break;
+                ++q_it;
+                // prologue: S_t(0)
+                uint32_t k_slot = kv_it % C::kStages;
+                if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
+                    break;
+                ++kv_it;
+                tc_fence_after();
+                for (int t = 0; t < nt; ++t)
+                    issue_s(t, k_slot);
+                mma_commit(bar(BB::kKVEmpty + k_slot));
+                if (U.n_kv == 1)
+                    mma_commit(bar(BB::kQEmpty));
+                for (int j = 0; j < U.n_kv && ok; ++j) {
+                    const uint32_t v_slot = kv_it % C::kStages;
+                    if (!wait(bar(BB::kKVFull + v_slot), (kv_it / C::kStages) & 1u))
+                        break;
+                    ++kv_it;
+                    const bool has_next = j + 1 < U.n_kv;
+                    for (int t = 0; t < nt && ok; ++t) {
+                        if (j == 0) {
+                            if (!wait(bar(BB::kOEmpty + t), (oe_it[t] & 1u) ^ 1u))
+                                break;
+                            ++oe_it[t];
+                        }
+                        if (!wait(bar(BB::kPFull + t), p_it[t] & 1u))
+                            break;
+                        ++p_it[t];
+                        tc_fence_after();
+                        issue_pv(t, v_slot, j > 0);
+                        if (has_next) {
+                            if (t == 0) {
+                                k_slot = kv_it % C::kStages;
+                                if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
+                                    break;
+                                ++kv_it;
+                                tc_fence_after();
+                            }
+                            issue_s(t, k_slot);
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(bar(BB::kKVEmpty + v_slot));
+                    if (has_next) {
+                        mma_commit(bar(BB::kKVEmpty + k_slot));
+                        if (j + 2 == U.n_kv)
+                            mma_commit(bar(BB::kQEmpty));
+                    }
+                }
+            }
+            // Every MMA this thread issued is complete before TMEM is released.
+            mma_commit(bar(BB::kMmaDone));
+            mbar_wait(bar(BB::kMmaDone), 0, abort_flag, kWaitLimitNs);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 4) >> 2;   // Q tile of this warpgroup
+        const int wq = warp & 3;         // TMEM lane quarter
+        const int rt = wq * 32 + lane;   // row within the Q tile = TMEM lane
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t tS = lane_base + (t ? C::kTmemS1 : C::kTmemS0);
+        const uint32_t tO = lane_base + (t ? C::kTmemO1 : C::kTmemO0);
+        const float scale = p.scale_log2;
+        uint32_t s_it = 0, pv_cnt = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int u = unit_at(r, cta, G);
+            if (u >= args.n_units)
+                break;
+            const Unit U = decode_unit(args, u);
+            if (U.n_kv == 0 || (t == 1 && !U.q1_valid)) {
+                // Nothing to accumulate: rows with no allowed key get O = 0 and lse = -inf.
+                const int row = U.q0 + t * kBM + rt;
+                if (U.n_kv == 0 && row < p.N) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(U.bh) * p.N + row) * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c)
+                        dst[c] = z;
+                    if (p.lse)
+                        p.lse[static_cast<size_t>(U.bh) * p.N + row] = -INFINITY;
+                }
+                continue;
+            }
+            const int row = U.q0 + t * kBM + rt;
+            const int tile_row0 = U.q0 + t * kBM;
+            float m_ref = -INFINITY; // reference max of the exponentials (log2 units)
+            float l = 0.f;
+            for (int j = 0; j < U.n_kv; ++j) {
+                if (!mbar_wait(bar(BB::kSFull + t), s_it & 1u, abort_flag, kWaitLimitNs)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                ++s_it;
+                tc_fence_after();
+                const int kv0 = j * kBN;
+                const bool need_mask = (kv0 + kBN > U.L) || (p.causal && kv0 + kBN - 1 > tile_row0);
+                int lim = U.L - kv0; // keys [kv0, kv0 + lim) are allowed for this row
+                if (p.causal)
+                    lim = min(lim, row - kv0 + 1);
+
+                // pass 1: row max of the scaled, masked scores
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + c * 32, v);
+                    #pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float x = __uint_as_float(v[e]) * scale;
+                        if (need_mask && c * 32 + e >= lim)
+                            x = -INFINITY;
+                        mx = fmaxf(mx, x);
+                    }
+                }
+                // lazy correction of the reference
+                if (mx > m_ref + kRescaleLog2) {
+                    const float alpha = ex2_approx(m_ref - mx);
+                    if (l > 0.f) {
+                        // O holds the PV products of earlier tiles: wait for the last one.
+                        if (!mbar_wait(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u, abort_flag, kWaitLimitNs)) {
+                            fail();
+                            ok = false;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(tO + c * 32, v);
+                            #pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            tmem_st32(tO + c * 32, v);
+                        }
+                        tmem_wait_st();
+                    }
+                    l *= alpha;
+                    m_ref = mx;
+                }
+                if (!ok)
+                    break;
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                const float neg_m = -m_use;
+
+                // pass 2: P = exp2(S * scale - m_ref) as fp16, written over S
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + c * 32, v);
+                                        uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), scale, neg_m));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), scale, neg_m));
+                        if (need_mask) {
+                            if (c * 32 + e >= lim)
+                                p0 = 0.f;
+                            if (c * 32 + e + 1 >= lim)
+                                p1 = 0.f;
+                        }
+                        rs += p0 + p1;
+                        pk[e >> 1] = pack_f16x2(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(BB::kPFull + t));
+                l += rs;
+                ++pv_cnt;
+            }
+            if (!ok)
+                break;
+            // epilogue: O / l -> fp16, logsumexp
+            if (!mbar_wait(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u, abort_flag, kWaitLimitNs)) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __half *orow = p.o + (static_cast<size_t>(U.bh) * p.N + row) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tO + c * 32, v);
+                                uint32_t h[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)
+                    h[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                if (row < p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                    dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
+                    dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(BB::kOEmpty + t));
+            if (p.lse && row < p.N)
+                p.lse[static_cast<size_t>(U.bh) * p.N + row] =
+                    l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem, C::kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [B*H, N, D] fp16 viewed as a 3-D tensor (D innermost); boxes of 128 rows x 64 columns,
+// 128-byte swizzle; rows past N read as zero.
+bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+std::mutex g_sm_mutex;
+
+cudaError_t sm_count(int *out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_sm_mutex);
+    if (!g_sm_count[dev]) {
+        err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess)
+            return err;
+    }
+    *out = g_sm_count[dev];
+    return cudaSuccess;
+}
+
+template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, unsigned int *status)
+{
+    using C = Cfg<D>;
+    const int BH = p.B * p.H;
+    CUtensorMap mq, mk, mv;
+    if (!encode_map(&mq, p.q, BH, p.N, D) || !encode_map(&mk, p.k, BH, p.N, D) ||
+        !encode_map(&mv, p.v, BH, p.N, D))
+        return cudaErrorInvalidValue;
+    TcArgs a;
+    a.p = p;
+    a.n_pairs = (p.N + 2 * kBM - 1) / (2 * kBM);
+    const long long units = static_cast<long long>(a.n_pairs) * BH;
+    if (units > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    a.n_units = static_cast<int>(units);
+    a.status = status;
+    int sms = 0;
+    cudaError_t err = sm_count(&sms);
+    if (err != cudaSuccess)
+        return err;
+    err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    const int grid = a.n_units < sms ? a.n_units : sms;
+    attn_fwd_tcgen05_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
+{
+    switch (p.d) {
+    case 64: return launch_d<64>(p, stream, status);
+    case 128: return launch_d<128>(p, stream, status);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 } // namespace attn

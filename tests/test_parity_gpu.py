@@ -19,7 +19,7 @@ from parity import compare, oracle_full, run_gpu, sample_rows
 pytestmark = pytest.mark.gpu
 
 # Kernels to check on every shape they support.
-KERNELS = ["warp_mma"]
+KERNELS = ["warp_mma", "tcgen05"]
 
 
 def kernels_for(d):
