@@ -324,6 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float scale = p.scale_log2;
         uint32_t s_it = 0, pv_cnt = 0;
         bool ok = true;
+        // tcgen05.ld/st are warp-collective (.sync.aligned): every branch around them, and
+        // every decision to give up, is made uniform across the warp first.
+        auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+            bool r = mbar_wait(b, parity, abort_flag, kWaitLimitNs);
+            r = __all_sync(0xffffffffu, r);
+            if (!r)
+                fail();
+            return r;
+        };
         for (int r = 0; ok; ++r) {
             const int u = unit_at(r, cta, G);
             if (u >= args.n_units)
@@ -348,8 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY; // reference max of the exponentials (log2 units)
             float l = 0.f;
             for (int j = 0; j < U.n_kv; ++j) {
-                if (!mbar_wait(bar(BB::kSFull + t), s_it & 1u, abort_flag, kWaitLimitNs)) {
-                    fail();
+                if (!wait_all(bar(BB::kSFull + t), s_it & 1u)) {
                     ok = false;
                     break;
                 }
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tS + c * 32, v);
-                    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         float x = __uint_as_float(v[e]) * scale;
                         if (need_mask && c * 32 + e >= lim)
@@ -375,32 +383,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mx = fmaxf(mx, x);
                     }
                 }
-                // lazy correction of the reference
-                if (mx > m_ref + kRescaleLog2) {
-                    const float alpha = ex2_approx(m_ref - mx);
-                    if (l > 0.f) {
+                // Lazy correction: a row moves its reference only when its max grew by more
+                // than 2^8; the warp rescales together when any of its rows does.
+                const bool want = mx > m_ref + kRescaleLog2;
+                if (__any_sync(0xffffffffu, want)) {
+                    const float alpha = want ? ex2_approx(m_ref - mx) : 1.f;
+                    if (__any_sync(0xffffffffu, want && l > 0.f)) {
                         // O holds the PV products of earlier tiles: wait for the last one.
-                        if (!mbar_wait(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u, abort_flag, kWaitLimitNs)) {
-                            fail();
+                        if (!wait_all(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u)) {
                             ok = false;
+                            break;
                         }
                         tc_fence_after();
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t v[32];
                             tmem_ld32(tO + c * 32, v);
-                            #pragma unroll
+#pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                             tmem_st32(tO + c * 32, v);
                         }
                         tmem_wait_st();
                     }
-                    l *= alpha;
-                    m_ref = mx;
+                    if (want) {
+                        l *= alpha;
+                        m_ref = mx;
+                    }
                 }
-                if (!ok)
-                    break;
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 const float neg_m = -m_use;
 
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tS + c * 32, v);
-                                        uint32_t pk[16];
+                    uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), scale, neg_m));
@@ -435,10 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok)
                 break;
             // epilogue: O / l -> fp16, logsumexp
-            if (!mbar_wait(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u, abort_flag, kWaitLimitNs)) {
-                fail();
+            if (!wait_all(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u))
                 break;
-            }
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __half *orow = p.o + (static_cast<size_t>(U.bh) * p.N + row) * D;
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(tO + c * 32, v);
-                                uint32_t h[16];
+                uint32_t h[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2)
                     h[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);

@@ -53,11 +53,14 @@ def test_small_shapes(shape):
         compare(o, lse, o_ref, lse_ref, what=f"{kern} {shape}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("scale", [0.05, 1.0, 2.5])
-def test_scales(scale):
-    q, k, v, _ = synth.draw(2, 2, 300, 64, seed=77)
+def test_scales(scale, d):
+    """Wide score ranges (scale 1.0 and 2.5) make the rows of one warp disagree about when to
+    move the softmax reference; small ones never move it after the first tile."""
+    q, k, v, _ = synth.draw(2, 2, 300, d, seed=77)
     o_ref, lse_ref = oracle_full(q, k, v, causal=True, sm_scale=scale)
-    for kern in kernels_for(64):
+    for kern in kernels_for(d):
         o, lse = run_gpu(q, k, v, causal=True, sm_scale=scale, path=kern)
         compare(o, lse, o_ref, lse_ref, what=f"{kern} scale={scale}")
 
