@@ -5,18 +5,21 @@
 // laid out for the Blackwell tensor core:
 //
 //   work unit   (batch*head, pair of 128-row Q tiles); a persistent grid of one CTA
-//               per SM walks the units heaviest-first in a snake order, so causal
-//               triangles spread evenly without any global counter.
-//   warp 0      TMA producer: Q0/Q1 once per unit, then K_j and V_j through a ring of
+//               per SM walks the units in a static order: heads are taken in blocks
+//               whose K/V fit comfortably in L2, and inside a block the units go
+//               heaviest-first (last query rows first under a causal mask) in a snake
+//               over the CTAs, so causal triangles spread evenly without any counter.
+//   warp 8      TMA producer: Q0/Q1 once per unit, then K_j and V_j through a ring of
 //               shared-memory stages (full/empty mbarriers with transaction counts).
 //               K/V tiles past the causal diagonal or past key_lengths[b] are never
 //               loaded (the block skip of "Engineering Decisions & Trade-offs" and the
 //               padding tile skip of the "cuda-reranker" README).
-//   warp 1      allocates TMEM and issues every tcgen05.mma from one thread:
+//   warp 9      allocates TMEM and issues every tcgen05.mma from one thread:
 //               S_t = Q_t K_j^T (fp16 x fp16 -> fp32 in TMEM) and O_t += P_t V_j with
 //               P_t read from TMEM; completion is signalled with tcgen05.commit.
-//   warps 4-7   softmax warpgroup for Q tile 0, warps 8-11 for Q tile 1: thread r owns
-//               TMEM lane r = query row r. Per K/V tile it reads the S row, scales,
+//   warps 0-3   softmax warpgroup for Q tile 0, warps 4-7 for Q tile 1: thread r owns
+//               TMEM lane r = query row r. Per K/V tile it reads the S row (one TMEM
+//               load of 128 columns), scales,
 //               masks, updates the running max m and normaliser l with exp2, and writes
 //               P (fp16) into TMEM over S. The accumulator O is rescaled only when the
 //               row max grows by more than 2^8 over the reference used so far (lazy
@@ -42,7 +45,16 @@ using namespace sm100;
 
 constexpr int kBM = 128;      // query rows per Q tile
 constexpr int kBN = 128;      // keys per K/V tile
-constexpr int kThreads = 384; // 12 warps
+constexpr int kThreads = 384; // 12 warps: softmax warpgroups 0 and 1, control warpgroup 2
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// Register split after launch: the softmax warpgroups hold a 128-column S row in
+// registers, the control warpgroup (TMA, MMA and two idle warps) needs few. The pool is
+// what the CTA launched with (threads x registers per thread); the host checks that
+// 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsControl fits in it before launching.
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr uint32_t kRegsControl = 88;
+constexpr int kRegPoolNeeded = 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsControl;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f; // lazy-correction threshold (log2 units)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -65,6 +77,7 @@ struct TcArgs {
     FwdParams p;
     int n_pairs; // ceil(N / 256)
     int n_units; // n_pairs * B * H
+    int head_block; // heads per L2 block of the unit order
     unsigned int *status;
 };
 
@@ -77,8 +90,13 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
 {
     const int BH = a.p.B * a.p.H;
     Unit U;
-    const int pair = a.n_pairs - 1 - u / BH; // the last query rows carry the most causal work
-    U.bh = u % BH;
+    const int per_block = a.head_block * a.n_pairs;
+    const int blk = u / per_block;
+    const int w = u - blk * per_block;
+    const int h0 = blk * a.head_block;
+    const int hb = min(a.head_block, BH - h0);
+    const int pair = a.n_pairs - 1 - w / hb; // the last query rows carry the most causal work
+    U.bh = h0 + w % hb;
     U.b = U.bh / a.p.H;
     U.q0 = pair * 2 * kBM;
     int L = a.p.N;
@@ -113,6 +131,91 @@ template <int D> struct Bars {
     static constexpr int kMmaDone = kOEmpty + 2;
     static constexpr int kCount = kMmaDone + 1;
 };
+
+// Row max of the scaled scores x_e = S_e * scale over the allowed columns e < lim
+// (MASK) or over all 128 columns. Without a mask the max is taken on the raw scores
+// (the min when the scale is negative) with three-input max and eight independent
+// chains, then scaled once.
+template <bool MASK>
+__device__ __forceinline__ float row_max(const uint32_t (&sv)[kBN], float scale, int lim)
+{
+    float acc[8];
+    if constexpr (!MASK) {
+        if (scale >= 0.f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[i] = fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[i + 8]));
+#pragma unroll
+            for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[i] = max3(acc[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
+            const float m = max3(max3(acc[0], acc[1], acc[2]), max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+            return m * scale;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[i] = fminf(__uint_as_float(sv[i]), __uint_as_float(sv[i + 8]));
+#pragma unroll
+            for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[i] = min3(acc[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
+            const float m = min3(min3(acc[0], acc[1], acc[2]), min3(acc[3], acc[4], acc[5]), fminf(acc[6], acc[7]));
+            return m * scale;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[i] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kBN; ++e) {
+            const float x = e < lim ? __uint_as_float(sv[e]) * scale : -INFINITY;
+            acc[e & 7] = fmaxf(acc[e & 7], x);
+        }
+        return max3(max3(acc[0], acc[1], acc[2]), max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+    }
+}
+
+// p_e = 2^(S_e * scale - m) rounded to fp16 pairs and stored to TMEM at tP (two halves
+// of 32 columns, so only half of the packed row is held in registers at a time);
+// returns sum_e p_e in fp32. Masked columns (e >= lim) give exactly 0. Pairs of lanes
+// use f32x2 arithmetic.
+template <bool MASK>
+__device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale, float neg_m, int lim,
+                                          uint32_t tP)
+{
+    const uint64_t sc2 = f2_pack(scale, scale);
+    const uint64_t nm2 = f2_pack(neg_m, neg_m);
+    uint64_t acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        acc[i] = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+            const int e = half * 64 + i;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+            if constexpr (MASK) {
+                if (e >= lim)
+                    x0 = -INFINITY;
+                if (e + 1 >= lim)
+                    x1 = -INFINITY;
+            }
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+            pk[i >> 1] = pack_f16x2(p0, p1);
+        }
+        tmem_st32(tP + half * 32, pk);
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+    f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+    return (a0 + a1) + (b0 + b1);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -154,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -171,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = gridDim.x;
     const int cta = blockIdx.x;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<kRegsControl>();
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
@@ -215,8 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<kRegsControl>();
         if (lane == 0) {
             uint32_t q_it = 0, kv_it = 0;
             uint32_t p_it[2] = {0, 0}, oe_it[2] = {0, 0};
@@ -313,9 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(BB::kMmaDone));
             mbar_wait(bar(BB::kMmaDone), 0, abort_flag, kWaitLimitNs);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 8) {
+        setmaxnreg_dec<kRegsControl>(); // idle warps of the control warpgroup
+    } else {
         // ------------------------------------------------------------ softmax warpgroups
-        const int t = (warp - 4) >> 2;   // Q tile of this warpgroup
+        setmaxnreg_inc<kRegsSoftmax>();
+        const int t = warp >> 2;         // Q tile of this warpgroup
         const int wq = warp & 3;         // TMEM lane quarter
         const int rt = wq * 32 + lane;   // row within the Q tile = TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -369,77 +477,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.causal)
                     lim = min(lim, row - kv0 + 1);
 
-                // pass 1: row max of the scaled, masked scores
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tS + c * 32, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float x = __uint_as_float(v[e]) * scale;
-                        if (need_mask && c * 32 + e >= lim)
-                            x = -INFINITY;
-                        mx = fmaxf(mx, x);
-                    }
-                }
+                uint32_t sv[kBN];
+                tmem_ld128(tS, sv);
+                const float mx = need_mask ? row_max<true>(sv, scale, lim) : row_max<false>(sv, scale, lim);
                 // Lazy correction: a row moves its reference only when its max grew by more
-                // than 2^8; the warp rescales together when any of its rows does.
+                // than 2^8 over it; O and l are rescaled together, so the result is exact.
                 const bool want = mx > m_ref + kRescaleLog2;
-                if (__any_sync(0xffffffffu, want)) {
-                    const float alpha = want ? ex2_approx(m_ref - mx) : 1.f;
-                    if (__any_sync(0xffffffffu, want && l > 0.f)) {
-                        // O holds the PV products of earlier tiles: wait for the last one.
-                        if (!wait_all(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t v[32];
-                            tmem_ld32(tO + c * 32, v);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                            tmem_st32(tO + c * 32, v);
-                        }
-                        tmem_wait_st();
-                    }
-                    if (want) {
-                        l *= alpha;
-                        m_ref = mx;
-                    }
-                }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                const float neg_m = -m_use;
+                const float alpha = want ? ex2_approx(m_ref - mx) : 1.f;
+                const float m_new = want ? mx : m_ref;
+                const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
 
-                // pass 2: P = exp2(S * scale - m_ref) as fp16, written over S
-                float rs = 0.f;
-#pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tS + c * 32, v);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), scale, neg_m));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), scale, neg_m));
-                        if (need_mask) {
-                            if (c * 32 + e >= lim)
-                                p0 = 0.f;
-                            if (c * 32 + e + 1 >= lim)
-                                p1 = 0.f;
-                        }
-                        rs += p0 + p1;
-                        pk[e >> 1] = pack_f16x2(p0, p1);
+                // P = exp2(S * scale - m_ref) as fp16, written over the first 64 columns of S
+                const float rs = need_mask ? exp_pack<true>(sv, scale, neg_m, lim, tS)
+                                           : exp_pack<false>(sv, scale, neg_m, lim, tS);
+                // O holds the PV products of earlier tiles; rescale it (after the last of
+                // them is done) before this tile's P is released to the MMA warp. The warp
+                // does it together when any of its rows needs it (tcgen05.ld/st are
+                // warp-collective).
+                if (__any_sync(0xffffffffu, want && l > 0.f)) {
+                    if (!wait_all(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u)) {
+                        ok = false;
+                        break;
                     }
-                    tmem_st16(tS + c * 16, pk);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tO + c * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(tO + c * 32, v);
+                    }
                 }
+                l = l * alpha + rs;
+                m_ref = m_new;
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(BB::kPFull + t));
-                l += rs;
                 ++pv_cnt;
             }
             if (!ok)
@@ -451,19 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __half *orow = p.o + (static_cast<size_t>(U.bh) * p.N + row) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tO + c * 32, v);
-                uint32_t h[16];
+            for (int half = 0; half < D / 64; ++half) {
+                uint32_t ov[64];
+                tmem_ld64(tO + half * 64, ov);
+                uint32_t h[32];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    h[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                for (int e = 0; e < 64; e += 2)
+                    h[e >> 1] = pack_f16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
                 if (row < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                    dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
-                    dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + half * 64);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
                 }
             }
             tc_fence_before();
@@ -477,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1)
+    if (warp == kMmaWarp)
         tmem_dealloc(tmem, C::kTmemCols);
 }
 
@@ -551,6 +625,11 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     if (units > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     a.n_units = static_cast<int>(units);
+    // Heads per block of the unit order: keep the K/V of the heads in flight within
+    // about 48 MB of L2, so the query-tile pairs of one head reuse its K/V from L2.
+    const long long kv_head = 4LL * p.N * D; // K and V of one head, fp16
+    long long hblk = (48LL << 20) / (kv_head > 0 ? kv_head : 1);
+    a.head_block = static_cast<int>(hblk < 1 ? 1 : (hblk > BH ? BH : hblk));
     a.status = status;
     int sms = 0;
     cudaError_t err = sm_count(&sms);
@@ -560,6 +639,13 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
                                C::kSmemBytes);
     if (err != cudaSuccess)
         return err;
+    // The register split inside the kernel must fit the pool the CTA is launched with.
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, attn_fwd_tcgen05_kernel<D>);
+    if (err != cudaSuccess)
+        return err;
+    if (static_cast<long long>(fa.numRegs) * kThreads < kRegPoolNeeded)
+        return cudaErrorInvalidConfiguration;
     const int grid = a.n_units < sms ? a.n_units : sms;
     attn_fwd_tcgen05_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv);
     return cudaGetLastError();
