@@ -36,7 +36,14 @@
 #include <cudaTypedefs.h>
 
 #include <math.h>
+#include <string.h>
+#include <algorithm>
+#include <map>
+#include <memory>
 #include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
 
 namespace attn {
 namespace {
@@ -62,7 +69,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 template <int D> struct Cfg {
     static constexpr int kBoxBytes = kBM * 128;       // one 128-row x 64-column fp16 TMA box
     static constexpr int kTileBytes = kBM * D * 2;    // a 128 x D fp16 tile
-    static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring depth
+    static constexpr int kStages = D == 128 ? 5 : 11; // K/V ring depth (fills the 227 KiB of shared memory)
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kOffQ = 0;
@@ -82,8 +89,21 @@ struct TcArgs {
 };
 
 struct Unit {
-    int bh, b, q0, L, n_kv;
-    bool q1_valid;
+    int bh, b, q0, L;
+    int n_kv;       // K/V tiles loaded for the unit (the larger of the two tile counts)
+    int n_kv_t[2];  // K/V tiles Q tile t attends to (0 when the tile lies past N)
+};
+
+// Static schedule computed on the host: CTA c processes the units
+// unit[off[c] .. off[c+1]) in that order (largest-first assignment to the least
+// loaded CTA, head block by head block). When `use` is 0 the CTAs walk the unit
+// order in a snake instead.
+constexpr int kMaxCtas = 256;
+constexpr int kMaxSchedUnits = 4096;
+struct SchedTable {
+    int use;
+    uint16_t off[kMaxCtas + 1];
+    uint16_t unit[kMaxSchedUnits];
 };
 
 __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
@@ -105,18 +125,48 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
         L = L < 0 ? 0 : (L > a.p.N ? a.p.N : L);
     }
     U.L = L;
-    int kv_end = L;
-    if (a.p.causal)
-        kv_end = min(kv_end, U.q0 + 2 * kBM);
-    U.n_kv = (kv_end + kBN - 1) / kBN;
-    U.q1_valid = U.q0 + kBM < a.p.N;
+    int kv_end0 = L, kv_end1 = L;
+    if (a.p.causal) {
+        kv_end0 = min(L, U.q0 + kBM); // Q tile 0 stops at its own diagonal
+        kv_end1 = min(L, U.q0 + 2 * kBM);
+    }
+    U.n_kv_t[0] = (kv_end0 + kBN - 1) / kBN;
+    U.n_kv_t[1] = U.q0 + kBM < a.p.N ? (kv_end1 + kBN - 1) / kBN : 0;
+    U.n_kv = max(U.n_kv_t[0], U.n_kv_t[1]);
     return U;
 }
+
+// K/V tile count of Q tile t, without indexing a local array by a runtime value.
+__device__ __forceinline__ int kv_tiles(const Unit &U, int t) { return t ? U.n_kv_t[1] : U.n_kv_t[0]; }
 
 // Unit of round r for CTA c: consecutive rounds walk the CTAs in opposite directions.
 __device__ __forceinline__ int unit_at(int r, int c, int G)
 {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+// The sequence of units of one CTA; every role of the CTA walks the same sequence.
+struct UnitCursor {
+    int i, end, r;
+};
+__device__ __forceinline__ UnitCursor first_unit(const SchedTable &s)
+{
+    UnitCursor c;
+    c.i = s.use ? s.off[blockIdx.x] : 0;
+    c.end = s.use ? s.off[blockIdx.x + 1] : 0;
+    c.r = 0;
+    return c;
+}
+__device__ __forceinline__ bool next_unit(const TcArgs &a, const SchedTable &s, UnitCursor &c, int &u)
+{
+    if (s.use) {
+        if (c.i >= c.end)
+            return false;
+        u = s.unit[c.i++];
+        return true;
+    }
+    u = unit_at(c.r++, blockIdx.x, gridDim.x);
+    return u < a.n_units;
 }
 
 // Barrier block layout (8 bytes each).
@@ -221,7 +271,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tcgen05_kernel(const TcArgs args, const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v)
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ SchedTable sched)
 {
     using C = Cfg<D>;
     using BB = Bars<D>;
@@ -271,8 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *args.status = kDevStatusTimeout;
     };
 
-    const int G = gridDim.x;
-    const int cta = blockIdx.x;
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
@@ -283,10 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm_v);
             uint32_t q_it = 0, kv_it = 0;
             bool ok = true;
-            for (int r = 0; ok; ++r) {
-                const int u = unit_at(r, cta, G);
-                if (u >= args.n_units)
-                    break;
+            UnitCursor cur = first_unit(sched);
+            int u;
+            while (ok && next_unit(args, sched, cur, u)) {
                 const Unit U = decode_unit(args, u);
                 if (U.n_kv == 0)
                     continue;
@@ -354,35 +402,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (accumulate || kk > 0) ? 1u : 0u);
                 mma_commit(bar(BB::kOReady + t));
             };
-            for (int r = 0; ok; ++r) {
-                const int u = unit_at(r, cta, G);
-                if (u >= args.n_units)
-                    break;
+            UnitCursor cur = first_unit(sched);
+            int u;
+            while (ok && next_unit(args, sched, cur, u)) {
                 const Unit U = decode_unit(args, u);
                 if (U.n_kv == 0)
                     continue;
-                const int nt = U.q1_valid ? 2 : 1;
                 if (!wait(bar(BB::kQFull), q_it & 1u))
                     break;
                 ++q_it;
-                // prologue: S_t(0)
+                // prologue: S_t(0) for every active tile
                 uint32_t k_slot = kv_it % C::kStages;
                 if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
                     break;
                 ++kv_it;
                 tc_fence_after();
-                for (int t = 0; t < nt; ++t)
-                    issue_s(t, k_slot);
+                for (int t = 0; t < 2; ++t)
+                    if (kv_tiles(U, t) > 0)
+                        issue_s(t, k_slot);
                 mma_commit(bar(BB::kKVEmpty + k_slot));
                 if (U.n_kv == 1)
                     mma_commit(bar(BB::kQEmpty));
+                // step j: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T; a tile whose
+                // causal range ends earlier drops out of the later steps.
                 for (int j = 0; j < U.n_kv && ok; ++j) {
                     const uint32_t v_slot = kv_it % C::kStages;
                     if (!wait(bar(BB::kKVFull + v_slot), (kv_it / C::kStages) & 1u))
                         break;
                     ++kv_it;
                     const bool has_next = j + 1 < U.n_kv;
-                    for (int t = 0; t < nt && ok; ++t) {
+                    bool k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= kv_tiles(U, t))
+                            continue;
                         if (j == 0) {
                             if (!wait(bar(BB::kOEmpty + t), (oe_it[t] & 1u) ^ 1u))
                                 break;
@@ -393,12 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++p_it[t];
                         tc_fence_after();
                         issue_pv(t, v_slot, j > 0);
-                        if (has_next) {
-                            if (t == 0) {
+                        if (j + 1 < kv_tiles(U, t)) {
+                            if (!k_ready) {
                                 k_slot = kv_it % C::kStages;
                                 if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
                                     break;
                                 ++kv_it;
+                                k_ready = true;
                                 tc_fence_after();
                             }
                             issue_s(t, k_slot);
@@ -408,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     mma_commit(bar(BB::kKVEmpty + v_slot));
                     if (has_next) {
+                        // the tile with the most K/V tiles always consumed K_{j+1} above
                         mma_commit(bar(BB::kKVEmpty + k_slot));
                         if (j + 2 == U.n_kv)
                             mma_commit(bar(BB::kQEmpty));
@@ -441,15 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fail();
             return r;
         };
-        for (int r = 0; ok; ++r) {
-            const int u = unit_at(r, cta, G);
-            if (u >= args.n_units)
-                break;
+        UnitCursor cur = first_unit(sched);
+        int u;
+        while (ok && next_unit(args, sched, cur, u)) {
             const Unit U = decode_unit(args, u);
-            if (U.n_kv == 0 || (t == 1 && !U.q1_valid)) {
-                // Nothing to accumulate: rows with no allowed key get O = 0 and lse = -inf.
+            const int n_kv = kv_tiles(U, t);
+            if (n_kv == 0) {
+                // Nothing to accumulate: rows with no allowed key get O = 0 and lse = -inf
+                // (rows past N, of a tile that lies beyond the sequence, are not written).
                 const int row = U.q0 + t * kBM + rt;
-                if (U.n_kv == 0 && row < p.N) {
+                if (row < p.N) {
                     uint4 z = make_uint4(0, 0, 0, 0);
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(U.bh) * p.N + row) * D);
 #pragma unroll
@@ -464,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tile_row0 = U.q0 + t * kBM;
             float m_ref = -INFINITY; // reference max of the exponentials (log2 units)
             float l = 0.f;
-            for (int j = 0; j < U.n_kv; ++j) {
+            for (int j = 0; j < n_kv; ++j) {
                 if (!wait_all(bar(BB::kSFull + t), s_it & 1u)) {
                     ok = false;
                     break;
@@ -610,6 +665,81 @@ cudaError_t sm_count(int *out)
     return cudaSuccess;
 }
 
+// Heads per block of the unit order: keep the K/V of the heads in flight within about
+// 48 MB of L2, so the query-tile pairs of one head reuse its K/V from L2.
+int head_block_for(int BH, int N, int D)
+{
+    const long long kv_head = 4LL * N * D; // K and V of one head, fp16
+    const long long hblk = (48LL << 20) / (kv_head > 0 ? kv_head : 1);
+    return static_cast<int>(hblk < 1 ? 1 : (hblk > BH ? BH : hblk));
+}
+
+// Largest-first assignment of the units to the least loaded CTA. The units are taken in
+// the device's unit order (head block by head block, heaviest pair first inside a
+// block), so every CTA works on the same head block at about the same time. The weight
+// of a unit is its count of (Q tile, K/V tile) steps plus a fixed per-unit cost; key
+// lengths are not known on the host and are taken as N.
+void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, int n_pairs, int grid)
+{
+    const int n_units = BH * n_pairs;
+    const int per_block = head_block * n_pairs;
+    using Slot = std::pair<long long, int>; // (load, cta)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int c = 0; c < grid; ++c)
+        heap.push({0, c});
+    std::vector<std::vector<uint16_t>> lists(grid);
+    for (int u = 0; u < n_units; ++u) {
+        const int blk = u / per_block;
+        const int w = u - blk * per_block;
+        const int hb = std::min(head_block, BH - blk * head_block);
+        const int pair = n_pairs - 1 - w / hb;
+        const int q0 = pair * 2 * kBM;
+        int e0 = N, e1 = N;
+        if (causal) {
+            e0 = std::min(N, q0 + kBM);
+            e1 = std::min(N, q0 + 2 * kBM);
+        }
+        const int n0 = (e0 + kBN - 1) / kBN;
+        const int n1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
+        const long long weight = n0 + n1 + 2;
+        Slot s = heap.top();
+        heap.pop();
+        lists[s.second].push_back(static_cast<uint16_t>(u));
+        heap.push({s.first + weight, s.second});
+    }
+    t.use = 1;
+    int k = 0;
+    for (int c = 0; c < grid; ++c) {
+        t.off[c] = static_cast<uint16_t>(k);
+        for (uint16_t u : lists[c])
+            t.unit[k++] = u;
+    }
+    t.off[grid] = static_cast<uint16_t>(k);
+}
+
+// Schedules are cached per shape (they depend on B*H, N, d, causal and the SM count only).
+std::mutex g_sched_mutex;
+std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
+
+std::shared_ptr<SchedTable> schedule_for(int BH, int N, int D, int causal, int head_block, int n_pairs,
+                                         int grid)
+{
+    auto key = std::make_tuple(BH, N, D, causal, grid);
+    std::lock_guard<std::mutex> lock(g_sched_mutex);
+    auto it = g_sched_cache.find(key);
+    if (it != g_sched_cache.end())
+        return it->second;
+    auto t = std::make_shared<SchedTable>();
+    memset(t.get(), 0, sizeof(SchedTable));
+    const long long n_units = static_cast<long long>(BH) * n_pairs;
+    if (grid <= kMaxCtas && n_units <= kMaxSchedUnits)
+        build_schedule(*t, BH, N, causal, head_block, n_pairs, grid);
+    if (g_sched_cache.size() >= 64)
+        g_sched_cache.clear();
+    g_sched_cache[key] = t;
+    return t;
+}
+
 template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
     using C = Cfg<D>;
@@ -625,11 +755,7 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     if (units > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     a.n_units = static_cast<int>(units);
-    // Heads per block of the unit order: keep the K/V of the heads in flight within
-    // about 48 MB of L2, so the query-tile pairs of one head reuse its K/V from L2.
-    const long long kv_head = 4LL * p.N * D; // K and V of one head, fp16
-    long long hblk = (48LL << 20) / (kv_head > 0 ? kv_head : 1);
-    a.head_block = static_cast<int>(hblk < 1 ? 1 : (hblk > BH ? BH : hblk));
+    a.head_block = head_block_for(BH, p.N, D);
     a.status = status;
     int sms = 0;
     cudaError_t err = sm_count(&sms);
@@ -647,7 +773,9 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     if (static_cast<long long>(fa.numRegs) * kThreads < kRegPoolNeeded)
         return cudaErrorInvalidConfiguration;
     const int grid = a.n_units < sms ? a.n_units : sms;
-    attn_fwd_tcgen05_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv);
+    std::shared_ptr<SchedTable> sched =
+        schedule_for(BH, p.N, D, p.causal, a.head_block, a.n_pairs, grid);
+    attn_fwd_tcgen05_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
     return cudaGetLastError();
 }
 
