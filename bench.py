@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05"])
+    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05", "short"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short-n", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)

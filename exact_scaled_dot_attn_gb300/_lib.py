@@ -17,7 +17,9 @@ ATTN_ERR_TIMEOUT = 5
 PATH_AUTO = 0
 PATH_WARP_MMA = 1
 PATH_TCGEN05 = 2
-PATHS = {"auto": PATH_AUTO, "warp_mma": PATH_WARP_MMA, "tcgen05": PATH_TCGEN05}
+PATH_SHORT = 3
+PATHS = {"auto": PATH_AUTO, "warp_mma": PATH_WARP_MMA, "tcgen05": PATH_TCGEN05,
+         "short": PATH_SHORT}
 
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 

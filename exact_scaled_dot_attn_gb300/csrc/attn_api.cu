@@ -84,7 +84,9 @@ extern "C" int attn_auto_path(int N, int d)
 {
     if (d != 32 && d != 64 && d != 128)
         return -1;
-    return (d != 32 && N > 256) ? ATTN_PATH_TCGEN05 : ATTN_PATH_WARP_MMA;
+    if (d <= 64 && N <= 256)
+        return ATTN_PATH_SHORT;
+    return d == 32 ? ATTN_PATH_WARP_MMA : ATTN_PATH_TCGEN05;
 }
 
 extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,
@@ -95,9 +97,12 @@ extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void 
     attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
         return st;
-    if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05)
+    if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
+        path != ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_TCGEN05 && d == 32)
+        return ATTN_ERR_UNSUPPORTED;
+    if (path == ATTN_PATH_SHORT && (N > 256 || d > 64))
         return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_AUTO)
         path = attn_auto_path(N, d);
@@ -119,11 +124,12 @@ extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void 
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
-    if (path == ATTN_PATH_TCGEN05) {
+    if (path == ATTN_PATH_TCGEN05 || path == ATTN_PATH_SHORT) {
         unsigned int *status = nullptr;
         err = status_word(&status);
         if (err == cudaSuccess)
-            err = attn::launch_tcgen05(p, s, status);
+            err = path == ATTN_PATH_TCGEN05 ? attn::launch_tcgen05(p, s, status)
+                                            : attn::launch_short(p, s, status);
     } else {
         err = attn::launch_warp_mma(p, s);
     }

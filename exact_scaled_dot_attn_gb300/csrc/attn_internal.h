@@ -26,6 +26,9 @@ cudaError_t launch_warp_mma(const FwdParams &p, cudaStream_t stream);
 // TMA + tcgen05/TMEM kernel (d in {64, 128}). `status` is the device status word.
 cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status);
 
+// Persistent short-sequence kernel (N <= 256, d in {32, 64}).
+cudaError_t launch_short(const FwdParams &p, cudaStream_t stream, unsigned int *status);
+
 // Status codes the kernels write into the device status word.
 constexpr unsigned int kDevStatusTimeout = 1u;
 

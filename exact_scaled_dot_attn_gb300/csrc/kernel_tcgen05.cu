@@ -46,6 +46,52 @@
 #include <vector>
 
 namespace attn {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+std::mutex g_sm_mutex;
+
+cudaError_t sm_count_locked(int *out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_sm_mutex);
+    if (!g_sm_count[dev]) {
+        err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess)
+            return err;
+    }
+    *out = g_sm_count[dev];
+    return cudaSuccess;
+}
+
+} // namespace
+
+// Multiprocessor count of the current device (cached per device).
+cudaError_t device_sm_count(int *out) { return sm_count_locked(out); }
+
 namespace {
 
 using namespace sm100;
@@ -610,21 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, C::kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 // [B*H, N, D] fp16 viewed as a 3-D tensor (D innermost); boxes of 128 rows x 64 columns,
 // 128-byte swizzle; rows past N read as zero.
 bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
@@ -641,28 +672,6 @@ bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];
-std::mutex g_sm_mutex;
-
-cudaError_t sm_count(int *out)
-{
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess)
-        return err;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_sm_mutex);
-    if (!g_sm_count[dev]) {
-        err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (err != cudaSuccess)
-            return err;
-    }
-    *out = g_sm_count[dev];
-    return cudaSuccess;
 }
 
 // Heads per block of the unit order: keep the K/V of the heads in flight within about
@@ -758,7 +767,7 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     a.head_block = head_block_for(BH, p.N, D);
     a.status = status;
     int sms = 0;
-    cudaError_t err = sm_count(&sms);
+    cudaError_t err = device_sm_count(&sms);
     if (err != cudaSuccess)
         return err;
     err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

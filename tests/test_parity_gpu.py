@@ -19,15 +19,25 @@ from parity import compare, oracle_full, run_gpu, sample_rows
 pytestmark = pytest.mark.gpu
 
 # Kernels to check on every shape they support.
-KERNELS = ["warp_mma", "tcgen05"]
+KERNELS = ["warp_mma", "tcgen05", "short"]
 
 
-def kernels_for(d):
-    return [k for k in KERNELS if not (k == "tcgen05" and d == 32)]
+def kernels_for(d, N=None):
+    out = []
+    for k in KERNELS:
+        if k == "tcgen05" and d == 32:
+            continue
+        if k == "short" and (d > 64 or (N is not None and N > 256)):
+            continue
+        out.append(k)
+    return out
 
 
 SMALL = [
     # B, H, N, d, causal, key_lengths
+    (3, 4, 256, 32, True, [256, 100, 3]),
+    (2, 3, 200, 64, True, [150, 200]),
+    (1, 2, 16, 64, False, None),
     (1, 1, 1, 64, False, None),
     (1, 2, 48, 32, False, None),
     (2, 3, 127, 64, True, None),
@@ -48,7 +58,7 @@ def test_small_shapes(shape):
     q, k, v, _ = synth.draw(B, H, N, d, seed=1000 + N + d)
     kl = None if kl is None else np.array(kl, np.int32)
     o_ref, lse_ref = oracle_full(q, k, v, causal=causal, key_lengths=kl)
-    for kern in kernels_for(d):
+    for kern in kernels_for(d, N):
         o, lse = run_gpu(q, k, v, causal=causal, key_lengths=kl, path=kern)
         compare(o, lse, o_ref, lse_ref, what=f"{kern} {shape}")
 
@@ -60,7 +70,7 @@ def test_scales(scale, d):
     move the softmax reference; small ones never move it after the first tile."""
     q, k, v, _ = synth.draw(2, 2, 300, d, seed=77)
     o_ref, lse_ref = oracle_full(q, k, v, causal=True, sm_scale=scale)
-    for kern in kernels_for(d):
+    for kern in kernels_for(d, 300):
         o, lse = run_gpu(q, k, v, causal=True, sm_scale=scale, path=kern)
         compare(o, lse, o_ref, lse_ref, what=f"{kern} scale={scale}")
 
@@ -79,7 +89,7 @@ def test_workload_full_rows(name):
     if w.ignore_padded_queries:
         i = np.arange(w.N)[None, None, :]
         row_mask = np.broadcast_to(i < kl[:, None, None], (w.B, w.H, w.N))
-    for kern in ["auto"] + kernels_for(w.d):
+    for kern in ["auto"] + kernels_for(w.d, w.N):
         o, lse = run_gpu(q, k, v, causal=w.causal, key_lengths=kl, path=kern)
         compare(o, lse, o_ref, lse_ref, row_mask=row_mask, what=f"{name} {kern}")
 
@@ -90,7 +100,7 @@ def test_workload_sampled_rows(name):
     rows = sample_rows(w.B, w.H, w.N, seed=w.seed, per_head=24)
     o_ref, lse_ref = oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal,
                                  key_lengths=kl, rows=rows)
-    for kern in ["auto"] + kernels_for(w.d):
+    for kern in ["auto"] + kernels_for(w.d, w.N):
         o, lse = run_gpu(q, k, v, causal=w.causal, key_lengths=kl, path=kern)
         o_s = o.reshape(-1, w.d)[rows]
         lse_s = lse.reshape(-1)[rows]
@@ -114,7 +124,7 @@ def test_uniform_keys_mean_of_v(d):
         n_allowed = np.minimum(np.arange(N) + 1, kl[0]) if causal else np.full(N, kl[0])
         csum = np.cumsum(v64, axis=2)
         mean = csum[:, :, n_allowed - 1] / n_allowed[None, None, :, None]
-        for kern in kernels_for(d):
+        for kern in kernels_for(d, N):
             o, _ = run_gpu(q, k, v, causal=causal, key_lengths=kl, path=kern)
             assert np.max(np.abs(o - mean)) <= 1e-2, (kern, causal)
 
@@ -130,7 +140,7 @@ def test_one_hot_selection(d):
         pi = np.array([rng.integers(0, i + 1) for i in range(N)]) if causal else rng.permutation(N)
         q = np.zeros((1, 1, N, d), np.float16)
         q[0, 0, np.arange(N), pi] = 20.0
-        for kern in kernels_for(d):
+        for kern in kernels_for(d, N):
             o, lse = run_gpu(q, k, v, causal=causal, sm_scale=1.0, path=kern)
             assert np.max(np.abs(o[0, 0] - v[0, 0, pi].astype(np.float64))) <= 2e-3, (kern, causal)
             assert np.max(np.abs(lse[0, 0] - 20.0)) <= 1e-3
@@ -141,7 +151,7 @@ def test_empty_rows_zero_output(d):
     """key_lengths = 0 empties every row of that batch: O = 0 and lse = -inf."""
     q, k, v, _ = synth.draw(2, 2, 130, d, seed=12)
     kl = np.array([0, 130], np.int32)
-    for kern in kernels_for(d):
+    for kern in kernels_for(d, 130):
         o, lse = run_gpu(q, k, v, causal=False, key_lengths=kl, path=kern)
         assert np.all(o[0] == 0.0) and np.all(lse[0] == -np.inf)
         assert np.all(np.isfinite(lse[1]))
@@ -149,9 +159,14 @@ def test_empty_rows_zero_output(d):
 
 def test_deterministic():
     q, k, v, _ = synth.draw(2, 4, 700, 128, seed=13)
-    for kern in kernels_for(128):
+    for kern in kernels_for(128, 700):
         o1, l1 = run_gpu(q, k, v, causal=True, path=kern)
         o2, l2 = run_gpu(q, k, v, causal=True, path=kern)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2), kern
+    q, k, v, kl = synth.draw(50, 12, 256, 32, seed=16, key_len_range=(64, 256))
+    for kern in kernels_for(32, 256):
+        o1, l1 = run_gpu(q, k, v, causal=False, key_lengths=kl, path=kern)
+        o2, l2 = run_gpu(q, k, v, causal=False, key_lengths=kl, path=kern)
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2), kern
 
 
