@@ -100,8 +100,6 @@ extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void 
     if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
         path != ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
-    if (path == ATTN_PATH_TCGEN05 && d == 32)
-        return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_SHORT && (N > 256 || d > 64))
         return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_AUTO)

@@ -1,4 +1,4 @@
-// TMA + tcgen05/TMEM attention forward for sm_103a (head dimension 64 or 128).
+// TMA + tcgen05/TMEM attention forward for sm_103a (head dimension 32, 64 or 128).
 //
 // The tiled online-softmax recurrence of "Self-Attention Kernel & Inference
 // Engine from Scratch" ("Online Softmax Formulation", "CUDA Kernel Structure"),
@@ -113,13 +113,17 @@ constexpr float kRescaleLog2 = 8.0f; // lazy-correction threshold (log2 units)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 template <int D> struct Cfg {
-    static constexpr int kBoxBytes = kBM * 128;       // one 128-row x 64-column fp16 TMA box
-    static constexpr int kTileBytes = kBM * D * 2;    // a 128 x D fp16 tile
-    static constexpr int kStages = D == 128 ? 5 : 11; // K/V ring depth (fills the 227 KiB of shared memory)
+    static constexpr int kBoxCols = D < 64 ? D : 64;   // columns per TMA box = one swizzle row
+    static constexpr int kRowBytes = kBoxCols * 2;     // 64 B (d = 32) or 128 B
+    static constexpr int kBoxBytes = kBM * kRowBytes;  // one 128-row box
+    static constexpr int kTileBytes = kBM * D * 2;     // a 128 x D fp16 tile (D / kBoxCols boxes)
+    static constexpr uint32_t kSwizzle = D < 64 ? 4u : 2u; // descriptor layout: 64 B / 128 B swizzle
+    static constexpr int kQStages = D == 128 ? 1 : 2;      // Q0/Q1 buffers (2: next unit prefetched)
+    static constexpr int kStages = D == 128 ? 5 : (D == 64 ? 9 : 16); // K/V ring depth
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = 2 * kTileBytes;
+    static constexpr int kOffKV = kQStages * 2 * kTileBytes;
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffBar + 1024 + 1024; // barriers + alignment slack
     static constexpr uint32_t kIdescS = idesc_f16_f32(kBM, kBN, 0, 0);
@@ -217,8 +221,9 @@ __device__ __forceinline__ bool next_unit(const TcArgs &a, const SchedTable &s, 
 
 // Barrier block layout (8 bytes each).
 template <int D> struct Bars {
-    static constexpr int kQFull = 0, kQEmpty = 1;
-    static constexpr int kKVFull = 2;
+    static constexpr int kQFull = 0;                              // [kQStages]
+    static constexpr int kQEmpty = kQFull + Cfg<D>::kQStages;     // [kQStages]
+    static constexpr int kKVFull = kQEmpty + Cfg<D>::kQStages;
     static constexpr int kKVEmpty = kKVFull + Cfg<D>::kStages;
     static constexpr int kSFull = kKVEmpty + Cfg<D>::kStages; // [2]
     static constexpr int kPFull = kSFull + 2;                 // [2]
@@ -338,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const FwdParams &p = args.p;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(BB::kQFull), 1);
-        mbar_init(bar(BB::kQEmpty), 1);
+        for (int s = 0; s < C::kQStages; ++s) {
+            mbar_init(bar(BB::kQFull + s), 1);
+            mbar_init(bar(BB::kQEmpty + s), 1);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(BB::kKVFull + s), 1);
             mbar_init(bar(BB::kKVEmpty + s), 1);
@@ -384,16 +391,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit U = decode_unit(args, u);
                 if (U.n_kv == 0)
                     continue;
-                if (!mbar_wait(bar(BB::kQEmpty), (q_it & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                const uint32_t qs = q_it % C::kQStages;
+                if (!mbar_wait(bar(BB::kQEmpty + qs), ((q_it / C::kQStages) & 1u) ^ 1u, abort_flag,
+                               kWaitLimitNs)) {
                     fail();
                     break;
                 }
                 ++q_it;
-                mbar_arrive_expect_tx(bar(BB::kQFull), 2 * C::kTileBytes);
+                mbar_arrive_expect_tx(bar(BB::kQFull + qs), 2 * C::kTileBytes);
                 for (int t = 0; t < 2; ++t)
-                    for (int bx = 0; bx < D / 64; ++bx)
-                        tma_load_3d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &tm_q,
-                                    bar(BB::kQFull), bx * 64, U.q0 + t * kBM, U.bh);
+                    for (int bx = 0; bx < D / C::kBoxCols; ++bx)
+                        tma_load_3d(sQ + (qs * 2 + t) * C::kTileBytes + bx * C::kBoxBytes, &tm_q,
+                                    bar(BB::kQFull + qs), bx * C::kBoxCols, U.q0 + t * kBM, U.bh);
                 for (int j = 0; j < U.n_kv && ok; ++j) {
                     for (int kv = 0; kv < 2; ++kv) {
                         const uint32_t slot = kv_it % C::kStages;
@@ -404,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(bar(BB::kKVFull + slot), C::kTileBytes);
-                        for (int bx = 0; bx < D / 64; ++bx)
+                        for (int bx = 0; bx < D / C::kBoxCols; ++bx)
                             tma_load_3d(sKV + slot * C::kTileBytes + bx * C::kBoxBytes,
-                                        kv == 0 ? &tm_k : &tm_v, bar(BB::kKVFull + slot), bx * 64,
-                                        j * kBN, U.bh);
+                                        kv == 0 ? &tm_k : &tm_v, bar(BB::kKVFull + slot),
+                                        bx * C::kBoxCols, j * kBN, U.bh);
                         ++kv_it;
                     }
                 }
@@ -427,14 +436,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return ok;
             };
+            uint32_t q_slot = 0;
+            // K-major operands (Q, K): 16 columns (32 bytes) per k-step inside a swizzle
+            // row; a new box every kBoxCols / 16 steps; 8-row groups kRowBytes * 8 apart.
             auto issue_s = [&](int t, uint32_t k_slot) {
-                const uint32_t qa = sQ + t * C::kTileBytes;
+                const uint32_t qa = sQ + (q_slot * 2 + t) * C::kTileBytes;
                 const uint32_t ka = sKV + k_slot * C::kTileBytes;
+                constexpr int kStepsPerBox = C::kBoxCols / 16;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + (t ? C::kTmemS1 : C::kTmemS0), smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(ka + off, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+                    const uint32_t off = (kk / kStepsPerBox) * C::kBoxBytes + (kk % kStepsPerBox) * 32;
+                    mma_ss(tmem + (t ? C::kTmemS1 : C::kTmemS0),
+                           smem_desc(qa + off, 16, 8 * C::kRowBytes, C::kSwizzle),
+                           smem_desc(ka + off, 16, 8 * C::kRowBytes, C::kSwizzle), C::kIdescS,
+                           kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(BB::kSFull + t));
             };
@@ -443,9 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t s_col = t ? C::kTmemS1 : C::kTmemS0;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
+                    // V is MN-major: 16 keys (rows) per k-step; the next 64 columns of d
+                    // (the next box) are kBoxBytes away; 8-key groups kRowBytes * 8 apart.
                     mma_ts(tmem + (t ? C::kTmemO1 : C::kTmemO0), tmem + s_col + kk * 8,
-                           smem_desc_sw128(va + kk * 2048, C::kBoxBytes, 1024), C::kIdescPV,
-                           (accumulate || kk > 0) ? 1u : 0u);
+                           smem_desc(va + kk * 16 * C::kRowBytes, C::kBoxBytes, 8 * C::kRowBytes,
+                                     C::kSwizzle),
+                           C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
                 mma_commit(bar(BB::kOReady + t));
             };
             UnitCursor cur = first_unit(sched);
@@ -454,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit U = decode_unit(args, u);
                 if (U.n_kv == 0)
                     continue;
-                if (!wait(bar(BB::kQFull), q_it & 1u))
+                q_slot = q_it % C::kQStages;
+                if (!wait(bar(BB::kQFull + q_slot), (q_it / C::kQStages) & 1u))
                     break;
                 ++q_it;
                 // prologue: S_t(0) for every active tile
@@ -468,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         issue_s(t, k_slot);
                 mma_commit(bar(BB::kKVEmpty + k_slot));
                 if (U.n_kv == 1)
-                    mma_commit(bar(BB::kQEmpty));
+                    mma_commit(bar(BB::kQEmpty + q_slot));
                 // step j: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T; a tile whose
                 // causal range ends earlier drops out of the later steps.
                 for (int j = 0; j < U.n_kv && ok; ++j) {
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the tile with the most K/V tiles always consumed K_{j+1} above
                         mma_commit(bar(BB::kKVEmpty + k_slot));
                         if (j + 2 == U.n_kv)
-                            mma_commit(bar(BB::kQEmpty));
+                            mma_commit(bar(BB::kQEmpty + q_slot));
                     }
                 }
             }
@@ -626,18 +645,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __half *orow = p.o + (static_cast<size_t>(U.bh) * p.N + row) * D;
+            constexpr int kChunk = D < 64 ? D : 64; // O columns per TMEM load
 #pragma unroll
-            for (int half = 0; half < D / 64; ++half) {
-                uint32_t ov[64];
-                tmem_ld64(tO + half * 64, ov);
-                uint32_t h[32];
+            for (int half = 0; half < D / kChunk; ++half) {
+                uint32_t ov[kChunk];
+                if constexpr (kChunk == 64)
+                    tmem_ld64(tO + half * 64, ov);
+                else
+                    tmem_ld32(tO, ov);
+                uint32_t h[kChunk / 2];
 #pragma unroll
-                for (int e = 0; e < 64; e += 2)
+                for (int e = 0; e < kChunk; e += 2)
                     h[e >> 1] = pack_f16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
                 if (row < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + half * 64);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
+                    for (int c = 0; c < kChunk / 8; ++c)
                         dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
                 }
             }
@@ -656,8 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// [B*H, N, D] fp16 viewed as a 3-D tensor (D innermost); boxes of 128 rows x 64 columns,
-// 128-byte swizzle; rows past N read as zero.
+// [B*H, N, D] fp16 viewed as a 3-D tensor (D innermost); boxes of 128 rows x 64 columns
+// with a 128-byte swizzle (x 32 columns with a 64-byte swizzle for D = 32); rows past N
+// read as zero.
 bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
 {
     auto enc = tensor_map_encoder();
@@ -667,10 +691,11 @@ bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(D < 64 ? D : 64), static_cast<cuuint32_t>(kBM), 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               D < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -793,6 +818,7 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
 cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
     switch (p.d) {
+    case 32: return launch_d<32>(p, stream, status);
     case 64: return launch_d<64>(p, stream, status);
     case 128: return launch_d<128>(p, stream, status);
     default: return cudaErrorInvalidValue;

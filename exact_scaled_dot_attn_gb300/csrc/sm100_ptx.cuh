@@ -127,17 +127,18 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor: start address, leading and stride byte
-// offsets (all >> 4), descriptor version 1 (bits 46-47), swizzle mode in bits
-// 61-63 (2 = 128-byte swizzle). The tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes)
+// offsets (all >> 4), descriptor version 1 (bits 46-47), layout in bits 61-63
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle). The swizzle pattern is applied to
+// absolute shared-memory addresses, so tiles start on 1024-byte boundaries.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout)
 {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(layout) << 61;
     return d;
 }
 

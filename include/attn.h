@@ -67,7 +67,7 @@ typedef enum {
 typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_WARP_MMA = 1, /* warp-level mma.sync tile kernel: every d, every N */
-    ATTN_PATH_TCGEN05 = 2,  /* TMA + tcgen05/TMEM warp-specialised kernel: d in {64, 128} */
+    ATTN_PATH_TCGEN05 = 2,  /* TMA + tcgen05/TMEM warp-specialised kernel: every d, every N */
     ATTN_PATH_SHORT = 3     /* persistent whole-head kernel: N <= 256, d in {32, 64} */
 } attn_path_t;
 
@@ -91,9 +91,8 @@ attn_status_t attn_fwd_lse(const void *q, const void *k, const void *v, void *o,
                            const int32_t *key_lengths, attn_stream_t stream);
 
 /* attn_fwd_lse with an explicit kernel choice (attn_path_t). A kernel asked for a
- * shape it does not take (ATTN_PATH_TCGEN05 with d = 32; ATTN_PATH_SHORT with
- * N > 256 or d = 128) returns ATTN_ERR_UNSUPPORTED. Used to check each kernel on
- * every shape it serves. */
+ * shape it does not take (ATTN_PATH_SHORT with N > 256 or d = 128) returns
+ * ATTN_ERR_UNSUPPORTED. Used to check each kernel on every shape it serves. */
 attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o, float *lse,
                             int B, int H, int N, int d, float sm_scale, int causal,
                             const int32_t *key_lengths, int path, attn_stream_t stream);

@@ -72,7 +72,8 @@ def call(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=8, d=64, scale=0.125, ca
     (dict(d=48), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(d=256), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(path=7), _lib.ATTN_ERR_UNSUPPORTED),
-    (dict(d=32, path=_lib.PATH_TCGEN05), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(d=128, path=_lib.PATH_SHORT), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(N=300, d=32, path=_lib.PATH_SHORT), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(q=A + 8), _lib.ATTN_ERR_MISALIGNED),
     (dict(o=A + 2), _lib.ATTN_ERR_MISALIGNED),
     (dict(lse=A + 2), _lib.ATTN_ERR_MISALIGNED),

@@ -25,8 +25,6 @@ KERNELS = ["warp_mma", "tcgen05", "short"]
 def kernels_for(d, N=None):
     out = []
     for k in KERNELS:
-        if k == "tcgen05" and d == 32:
-            continue
         if k == "short" and (d > 64 or (N is not None and N > 256)):
             continue
         out.append(k)
