@@ -437,32 +437,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return ok;
             };
             uint32_t q_slot = 0;
-            // K-major operands (Q, K): 16 columns (32 bytes) per k-step inside a swizzle
-            // row; a new box every kBoxCols / 16 steps; 8-row groups kRowBytes * 8 apart.
+            // Shared-memory descriptors, built once: the high word (stride byte offset,
+            // version, swizzle layout) is the same for every operand; the low word is
+            // (start address >> 4) | (leading byte offset >> 4) << 16, so stepping through
+            // a tile is one add per instruction. Addresses stay below 2^18, so the start
+            // field never carries into the leading-offset field.
+            constexpr uint32_t kDescHi = ((8 * C::kRowBytes) >> 4) | (1u << 14) | (C::kSwizzle << 29);
+            constexpr uint32_t kLboK = (16u >> 4) << 16;                            // K-major: unused
+            constexpr uint32_t kLboV = (static_cast<uint32_t>(C::kBoxBytes) >> 4) << 16; // next 64 columns of d
+            auto desc = [](uint32_t lo) -> uint64_t {
+                return (static_cast<uint64_t>(kDescHi) << 32) | lo;
+            };
+            // S_t = Q_t K^T: K-major operands, 16 columns (32 bytes) per k-step inside a
+            // swizzle row, a new box every kBoxCols / 16 steps.
             auto issue_s = [&](int t, uint32_t k_slot) {
-                const uint32_t qa = sQ + (q_slot * 2 + t) * C::kTileBytes;
-                const uint32_t ka = sKV + k_slot * C::kTileBytes;
+                const uint32_t qlo = ((sQ + (q_slot * 2 + t) * C::kTileBytes) >> 4) | kLboK;
+                const uint32_t klo = ((sKV + k_slot * C::kTileBytes) >> 4) | kLboK;
+                const uint32_t d_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
                 constexpr int kStepsPerBox = C::kBoxCols / 16;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / kStepsPerBox) * C::kBoxBytes + (kk % kStepsPerBox) * 32;
-                    mma_ss(tmem + (t ? C::kTmemS1 : C::kTmemS0),
-                           smem_desc(qa + off, 16, 8 * C::kRowBytes, C::kSwizzle),
-                           smem_desc(ka + off, 16, 8 * C::kRowBytes, C::kSwizzle), C::kIdescS,
-                           kk > 0 ? 1u : 0u);
+                    constexpr int kBox16 = C::kBoxBytes >> 4;
+                    const uint32_t off = (kk / kStepsPerBox) * kBox16 + (kk % kStepsPerBox) * 2;
+                    mma_ss(d_tmem, desc(qlo + off), desc(klo + off), C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(BB::kSFull + t));
             };
+            // O_t += P_t V: P from TMEM (8 columns = 16 fp16 keys per k-step); V is MN-major,
+            // 16 keys (rows) per k-step.
             auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
-                const uint32_t va = sKV + v_slot * C::kTileBytes;
-                const uint32_t s_col = t ? C::kTmemS1 : C::kTmemS0;
+                const uint32_t vlo = ((sKV + v_slot * C::kTileBytes) >> 4) | kLboV;
+                const uint32_t a_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
+                const uint32_t d_tmem = tmem + (t ? C::kTmemO1 : C::kTmemO0);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    // V is MN-major: 16 keys (rows) per k-step; the next 64 columns of d
-                    // (the next box) are kBoxBytes away; 8-key groups kRowBytes * 8 apart.
-                    mma_ts(tmem + (t ? C::kTmemO1 : C::kTmemO0), tmem + s_col + kk * 8,
-                           smem_desc(va + kk * 16 * C::kRowBytes, C::kBoxBytes, 8 * C::kRowBytes,
-                                     C::kSwizzle),
+                    mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((16 * C::kRowBytes) >> 4)),
                            C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
                 mma_commit(bar(BB::kOReady + t));
             };
