@@ -102,12 +102,15 @@ constexpr int kThreads = 384; // 12 warps: softmax warpgroups 0 and 1, control w
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 // Register split after launch: the softmax warpgroups hold a 128-column S row in
-// registers, the control warpgroup (TMA, MMA and two idle warps) needs few. The pool is
+// registers, the control warpgroup (TMA, MMA and two idle warps) needs few; at d = 128
+// the unrolled MMA issue of the control warpgroup needs more than at d <= 64. The pool is
 // what the CTA launched with (threads x registers per thread); the host checks that
-// 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsControl fits in it before launching.
-constexpr uint32_t kRegsSoftmax = 192;
-constexpr uint32_t kRegsControl = 88;
-constexpr int kRegPoolNeeded = 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsControl;
+// 8 * 32 * softmax + 4 * 32 * control fits in it before launching.
+template <int D> struct RegSplit {
+    static constexpr uint32_t kSoftmax = D == 128 ? 192 : 200;
+    static constexpr uint32_t kControl = D == 128 ? 88 : 72;
+    static constexpr int kPoolNeeded = 8 * 32 * kSoftmax + 4 * 32 * kControl;
+};
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f; // lazy-correction threshold (log2 units)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -233,58 +236,62 @@ template <int D> struct Bars {
     static constexpr int kCount = kMmaDone + 1;
 };
 
-// Row max of the scaled scores x_e = S_e * scale over the allowed columns e < lim
-// (MASK) or over all 128 columns. Without a mask the max is taken on the raw scores
-// (the min when the scale is negative) with three-input max and eight independent
-// chains, then scaled once.
-template <bool MASK>
-__device__ __forceinline__ float row_max(const uint32_t (&sv)[kBN], float scale, int lim)
+// Column chunks of the S row: the allowed columns of a row are a prefix e < lim (key
+// padding and the causal diagonal both cut a row at one column), so every 32-column chunk
+// is fully allowed, fully masked, or the single boundary chunk. Only the boundary chunk
+// pays for per-element masking; fully masked chunks cost nothing.
+constexpr int kChunkCols = 32;
+
+// Max (min when `neg`) of the raw scores of one fully allowed chunk: three-input max
+// over eight independent chains.
+template <bool NEG>
+__device__ __forceinline__ float chunk_extreme(const uint32_t (&sv)[kBN], int c)
 {
     float acc[8];
-    if constexpr (!MASK) {
-        if (scale >= 0.f) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[i] = fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[i + 8]));
+    for (int i = 0; i < 8; ++i)
+        acc[i] = NEG ? fminf(__uint_as_float(sv[c * 32 + i]), __uint_as_float(sv[c * 32 + 8 + i]))
+                     : fmaxf(__uint_as_float(sv[c * 32 + i]), __uint_as_float(sv[c * 32 + 8 + i]));
 #pragma unroll
-            for (int e = 16; e < kBN; e += 16)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[i] = max3(acc[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
-            const float m = max3(max3(acc[0], acc[1], acc[2]), max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
-            return m * scale;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[i] = fminf(__uint_as_float(sv[i]), __uint_as_float(sv[i + 8]));
-#pragma unroll
-            for (int e = 16; e < kBN; e += 16)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[i] = min3(acc[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
-            const float m = min3(min3(acc[0], acc[1], acc[2]), min3(acc[3], acc[4], acc[5]), fminf(acc[6], acc[7]));
-            return m * scale;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            acc[i] = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < kBN; ++e) {
-            const float x = e < lim ? __uint_as_float(sv[e]) * scale : -INFINITY;
-            acc[e & 7] = fmaxf(acc[e & 7], x);
-        }
-        return max3(max3(acc[0], acc[1], acc[2]), max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
-    }
+    for (int i = 0; i < 8; ++i)
+        acc[i] = NEG ? min3(acc[i], __uint_as_float(sv[c * 32 + 16 + i]), __uint_as_float(sv[c * 32 + 24 + i]))
+                     : max3(acc[i], __uint_as_float(sv[c * 32 + 16 + i]), __uint_as_float(sv[c * 32 + 24 + i]));
+    return NEG ? min3(min3(acc[0], acc[1], acc[2]), min3(acc[3], acc[4], acc[5]), fminf(acc[6], acc[7]))
+               : max3(max3(acc[0], acc[1], acc[2]), max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
 }
 
-// p_e = 2^(S_e * scale - m) rounded to fp16 pairs and stored to TMEM at tP (two halves
-// of 32 columns, so only half of the packed row is held in registers at a time);
-// returns sum_e p_e in fp32. Masked columns (e >= lim) give exactly 0. Pairs of lanes
-// use f32x2 arithmetic.
-template <bool MASK>
-__device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale, float neg_m, int lim,
-                                          uint32_t tP)
+// Row max of the scaled scores over a fully allowed row: the extreme of the raw scores
+// (the min when the scale is negative) by three-input max over eight independent
+// chains, scaled once.
+__device__ __forceinline__ float row_max_full(const uint32_t (&sv)[kBN], float scale)
+{
+    float acc[8];
+    if (scale >= 0.f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[i] = fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[i + 8]));
+#pragma unroll
+        for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[i] = max3(acc[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
+        return max3(max3(acc[0], acc[1], acc[2]), max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7])) * scale;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = fminf(__uint_as_float(sv[i]), __uint_as_float(sv[i + 8]));
+#pragma unroll
+    for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[i] = min3(acc[i], __uint_as_float(sv[e + i]), __uint_as_float(sv[e + 8 + i]));
+    return min3(min3(acc[0], acc[1], acc[2]), min3(acc[3], acc[4], acc[5]), fminf(acc[6], acc[7])) * scale;
+}
+
+// p_e = 2^(S_e * scale - m) over a fully allowed row, rounded to fp16 pairs and stored to
+// TMEM at tP in two halves of 32 columns; returns sum_e p_e in fp32 (f32x2 arithmetic).
+__device__ __forceinline__ float exp_pack_full(const uint32_t (&sv)[kBN], float scale, float neg_m,
+                                               uint32_t tP)
 {
     const uint64_t sc2 = f2_pack(scale, scale);
     const uint64_t nm2 = f2_pack(neg_m, neg_m);
@@ -300,15 +307,86 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
             const int e = half * 64 + i;
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
-            if constexpr (MASK) {
-                if (e >= lim)
-                    x0 = -INFINITY;
-                if (e + 1 >= lim)
-                    x1 = -INFINITY;
-            }
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
             pk[i >> 1] = pack_f16x2(p0, p1);
+        }
+        tmem_st32(tP + half * 32, pk);
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+    f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+    return (a0 + a1) + (b0 + b1);
+}
+
+// Row max of the scaled scores x_e = S_e * scale over the allowed columns e < lim
+// (lim >= 128: the whole row). Fully allowed chunks take the extreme of the raw scores
+// (the min when the scale is negative) and scale it once.
+__device__ __forceinline__ float row_max(const uint32_t (&sv)[kBN], float scale, int lim)
+{
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kBN / kChunkCols; ++c) {
+        if (lim >= (c + 1) * kChunkCols) {
+            const float r = scale >= 0.f ? chunk_extreme<false>(sv, c) : chunk_extreme<true>(sv, c);
+            m = fmaxf(m, r * scale);
+        } else if (lim > c * kChunkCols) {
+#pragma unroll
+            for (int i = 0; i < kChunkCols; ++i) {
+                const int e = c * kChunkCols + i;
+                const float x = e < lim ? __uint_as_float(sv[e]) * scale : -INFINITY;
+                m = fmaxf(m, x);
+            }
+        }
+    }
+    return m;
+}
+
+// p_e = 2^(S_e * scale - m) for the allowed columns e < lim, 0 elsewhere, rounded to fp16
+// pairs and stored to TMEM at tP (two halves of 32 columns, so only half of the packed
+// row is held in registers at a time); returns sum_e p_e in fp32. Pairs of lanes use
+// f32x2 arithmetic; fully masked chunks store zeros without evaluating any exponential.
+__device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale, float neg_m, int lim,
+                                          uint32_t tP)
+{
+    const uint64_t sc2 = f2_pack(scale, scale);
+    const uint64_t nm2 = f2_pack(neg_m, neg_m);
+    uint64_t acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        acc[i] = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c = half * 2 + cc;
+            if (lim >= (c + 1) * kChunkCols) {
+#pragma unroll
+                for (int i = 0; i < kChunkCols; i += 2) {
+                    const int e = c * kChunkCols + i;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+                    pk[cc * 16 + (i >> 1)] = pack_f16x2(p0, p1);
+                }
+            } else if (lim > c * kChunkCols) {
+#pragma unroll
+                for (int i = 0; i < kChunkCols; i += 2) {
+                    const int e = c * kChunkCols + i;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+                    const float p0 = e < lim ? ex2_approx(x0) : 0.f;
+                    const float p1 = e + 1 < lim ? ex2_approx(x1) : 0.f;
+                    acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+                    pk[cc * 16 + (i >> 1)] = pack_f16x2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[cc * 16 + i] = 0u;
+            }
         }
         tmem_st32(tP + half * 32, pk);
     }
@@ -378,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        setmaxnreg_dec<kRegsControl>();
+        setmaxnreg_dec<RegSplit<D>::kControl>();
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
@@ -424,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        setmaxnreg_dec<kRegsControl>();
+        setmaxnreg_dec<RegSplit<D>::kControl>();
         if (lane == 0) {
             uint32_t q_it = 0, kv_it = 0;
             uint32_t p_it[2] = {0, 0}, oe_it[2] = {0, 0};
@@ -547,10 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bar(BB::kMmaDone), 0, abort_flag, kWaitLimitNs);
         }
     } else if (warp >= 8) {
-        setmaxnreg_dec<kRegsControl>(); // idle warps of the control warpgroup
+        setmaxnreg_dec<RegSplit<D>::kControl>(); // idle warps of the control warpgroup
     } else {
         // ------------------------------------------------------------ softmax warpgroups
-        setmaxnreg_inc<kRegsSoftmax>();
+        setmaxnreg_inc<RegSplit<D>::kSoftmax>();
         const int t = warp >> 2;         // Q tile of this warpgroup
         const int wq = warp & 3;         // TMEM lane quarter
         const int rt = wq * 32 + lane;   // row within the Q tile = TMEM lane
@@ -608,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 uint32_t sv[kBN];
                 tmem_ld128(tS, sv);
-                const float mx = need_mask ? row_max<true>(sv, scale, lim) : row_max<false>(sv, scale, lim);
+                const float mx = need_mask ? row_max(sv, scale, lim) : row_max_full(sv, scale);
                 // Lazy correction: a row moves its reference only when its max grew by more
                 // than 2^8 over it; O and l are rescaled together, so the result is exact.
                 const bool want = mx > m_ref + kRescaleLog2;
@@ -617,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
 
                 // P = exp2(S * scale - m_ref) as fp16, written over the first 64 columns of S
-                const float rs = need_mask ? exp_pack<true>(sv, scale, neg_m, lim, tS)
-                                           : exp_pack<false>(sv, scale, neg_m, lim, tS);
+                const float rs = need_mask ? exp_pack(sv, scale, neg_m, lim, tS)
+                                           : exp_pack_full(sv, scale, neg_m, tS);
                 // O holds the PV products of earlier tiles; rescale it (after the last of
                 // them is done) before this tile's P is released to the MMA warp. The warp
                 // does it together when any of its rows needs it (tcgen05.ld/st are
@@ -813,7 +891,7 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     err = cudaFuncGetAttributes(&fa, attn_fwd_tcgen05_kernel<D>);
     if (err != cudaSuccess)
         return err;
-    if (static_cast<long long>(fa.numRegs) * kThreads < kRegPoolNeeded)
+    if (static_cast<long long>(fa.numRegs) * kThreads < RegSplit<D>::kPoolNeeded)
         return cudaErrorInvalidConfiguration;
     const int grid = a.n_units < sms ? a.n_units : sms;
     std::shared_ptr<SchedTable> sched =
