@@ -107,8 +107,8 @@ constexpr int kMmaWarp = 9;
 // what the CTA launched with (threads x registers per thread); the host checks that
 // 8 * 32 * softmax + 4 * 32 * control fits in it before launching.
 template <int D> struct RegSplit {
-    static constexpr uint32_t kSoftmax = D == 128 ? 192 : 200;
-    static constexpr uint32_t kControl = D == 128 ? 88 : 72;
+    static constexpr uint32_t kSoftmax = 200;
+    static constexpr uint32_t kControl = D == 128 ? 96 : 72;
     static constexpr int kPoolNeeded = 8 * 32 * kSoftmax + 4 * 32 * kControl;
 };
 constexpr float kLn2 = 0.6931471805599453f;
@@ -220,6 +220,33 @@ __device__ __forceinline__ bool next_unit(const TcArgs &a, const SchedTable &s, 
     }
     u = unit_at(c.r++, blockIdx.x, gridDim.x);
     return u < a.n_units;
+}
+
+// The CTA's units, decoded one ahead: taking a unit starts decoding the following one,
+// so its key-length load is in flight while the taken unit is processed.
+struct UnitStream {
+    UnitCursor cur;
+    bool has;
+    Unit next;
+};
+__device__ __forceinline__ void stream_init(UnitStream &st, const TcArgs &a, const SchedTable &s)
+{
+    st.cur = first_unit(s);
+    int u;
+    st.has = next_unit(a, s, st.cur, u);
+    if (st.has)
+        st.next = decode_unit(a, u);
+}
+__device__ __forceinline__ bool stream_take(UnitStream &st, const TcArgs &a, const SchedTable &s, Unit &U)
+{
+    if (!st.has)
+        return false;
+    U = st.next;
+    int u;
+    st.has = next_unit(a, s, st.cur, u);
+    if (st.has)
+        st.next = decode_unit(a, u);
+    return true;
 }
 
 // Barrier block layout (8 bytes each).
@@ -463,10 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm_v);
             uint32_t q_it = 0, kv_it = 0;
             bool ok = true;
-            UnitCursor cur = first_unit(sched);
-            int u;
-            while (ok && next_unit(args, sched, cur, u)) {
-                const Unit U = decode_unit(args, u);
+            UnitStream us;
+            stream_init(us, args, sched);
+            Unit U;
+            while (ok && stream_take(us, args, sched, U)) {
                 if (U.n_kv == 0)
                     continue;
                 const uint32_t qs = q_it % C::kQStages;
@@ -553,10 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
                 mma_commit(bar(BB::kOReady + t));
             };
-            UnitCursor cur = first_unit(sched);
-            int u;
-            while (ok && next_unit(args, sched, cur, u)) {
-                const Unit U = decode_unit(args, u);
+            UnitStream us;
+            stream_init(us, args, sched);
+            Unit U;
+            while (ok && stream_take(us, args, sched, U)) {
                 if (U.n_kv == 0)
                     continue;
                 q_slot = q_it % C::kQStages;
@@ -647,10 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fail();
             return r;
         };
-        UnitCursor cur = first_unit(sched);
-        int u;
-        while (ok && next_unit(args, sched, cur, u)) {
-            const Unit U = decode_unit(args, u);
+        UnitStream us;
+        stream_init(us, args, sched);
+        Unit U;
+        while (ok && stream_take(us, args, sched, U)) {
             const int n_kv = kv_tiles(U, t);
             if (n_kv == 0) {
                 // Nothing to accumulate: rows with no allowed key get O = 0 and lse = -inf
