@@ -23,11 +23,19 @@ PATHS = {"auto": PATH_AUTO, "warp_mma": PATH_WARP_MMA, "tcgen05": PATH_TCGEN05,
 
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 
+
+class DebugOpts(ctypes.Structure):
+    """attn_debug_opts_t of include/attn.h."""
+    _fields_ = [("wait_limit_ns", ctypes.c_uint64), ("inject_missing_arrive", ctypes.c_int)]
+
+
 # name -> (restype, argtypes); every function include/attn.h declares.
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
     "attn_fwd_lse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
     "attn_fwd_path": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_fwd_debug": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i,
+                            ctypes.POINTER(DebugOpts), _vp]),
     "attn_auto_path": (_i, [_i, _i]),
     "attn_status_str": (ctypes.c_char_p, [_i]),
     "attn_read_device_status": (_i, [_vp]),

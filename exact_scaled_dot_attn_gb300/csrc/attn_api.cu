@@ -89,10 +89,10 @@ extern "C" int attn_auto_path(int N, int d)
     return d == 32 ? ATTN_PATH_WARP_MMA : ATTN_PATH_TCGEN05;
 }
 
-extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,
-                                       float *lse, int B, int H, int N, int d, float sm_scale,
-                                       int causal, const int32_t *key_lengths, int path,
-                                       attn_stream_t stream)
+extern "C" attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *o,
+                                        float *lse, int B, int H, int N, int d, float sm_scale,
+                                        int causal, const int32_t *key_lengths, int path,
+                                        const attn_debug_opts_t *opts, attn_stream_t stream)
 {
     attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
@@ -119,6 +119,8 @@ extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void 
     p.sm_scale = sm_scale;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.causal = causal;
+    p.wait_limit_ns = (opts && opts->wait_limit_ns) ? opts->wait_limit_ns : attn::kDefaultWaitLimitNs;
+    p.inject_missing_arrive = opts ? (opts->inject_missing_arrive != 0) : 0;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
@@ -132,6 +134,15 @@ extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void 
         err = attn::launch_warp_mma(p, s);
     }
     return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,
+                                       float *lse, int B, int H, int N, int d, float sm_scale,
+                                       int causal, const int32_t *key_lengths, int path,
+                                       attn_stream_t stream)
+{
+    return attn_fwd_debug(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths, path, nullptr,
+                          stream);
 }
 
 extern "C" attn_status_t attn_fwd_lse(const void *q, const void *k, const void *v, void *o,

@@ -18,7 +18,12 @@ struct FwdParams {
     float sm_scale;
     float scale_log2; // sm_scale * log2(e): scores are exponentiated with exp2
     int causal;
+    unsigned long long wait_limit_ns; // bound of every on-chip wait (nonzero)
+    int inject_missing_arrive;        // self-test: withhold the first "P ready" arrival
 };
+
+// Default bound of an on-chip wait.
+constexpr unsigned long long kDefaultWaitLimitNs = 4000000000ull;
 
 // Warp-level mma.sync kernel (every d in {32, 64, 128}, every N).
 cudaError_t launch_warp_mma(const FwdParams &p, cudaStream_t stream);

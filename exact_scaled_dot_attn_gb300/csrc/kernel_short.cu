@@ -36,7 +36,6 @@ constexpr int kMaxN = 256;   // longest sequence this kernel takes
 constexpr int kBoxRows = 64; // rows per TMA box
 constexpr int kWarps = kMaxN / 16;
 constexpr int kThreads = kWarps * 32;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 template <int D> struct ShortCfg {
     static constexpr int kTileBytes = kMaxN * D * 2; // a resident [256][D] fp16 tile
@@ -115,11 +114,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bh >= n_heads)
             break;
         const uint32_t bar = bar0 + 8 * (k & 1);
-        bool ok = sm100::mbar_wait(bar, (k >> 1) & 1, abort_flag, kWaitLimitNs);
+        bool ok = sm100::mbar_wait(bar, (k >> 1) & 1, abort_flag, p.wait_limit_ns);
         ok = __syncthreads_and(ok);
         if (!ok) {
-            if (tid == 0)
+            if (tid == 0) {
                 *status = kDevStatusTimeout;
+                // The two stages issued last (heads k and k + 1) may still be loading: let
+                // them land, bounded by time only, before the CTA leaves.
+                for (int kk = k; kk < k + 2; ++kk)
+                    if (static_cast<int>(blockIdx.x) + kk * static_cast<int>(gridDim.x) < n_heads)
+                        sm100::mbar_wait(bar0 + 8 * (kk & 1), (kk >> 1) & 1, nullptr, p.wait_limit_ns);
+            }
             break;
         }
         __half *sQ = reinterpret_cast<__half *>(smem + (k & 1) * C::kStageBytes);

@@ -113,7 +113,6 @@ template <int D> struct RegSplit {
 };
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f; // lazy-correction threshold (log2 units)
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 template <int D> struct Cfg {
     static constexpr int kBoxCols = D < 64 ? D : 64;   // columns per TMA box = one swizzle row
@@ -446,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const FwdParams &p = args.p;
+    const uint64_t kWaitLimitNs = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kQStages; ++s) {
@@ -526,6 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // Loads still in flight land before the CTA may leave (after an abort): wait,
+            // bounded by time only, for the latest phase of every slot that was filled.
+            for (uint32_t i = q_it > C::kQStages ? q_it - C::kQStages : 0; i < q_it; ++i)
+                mbar_wait(bar(BB::kQFull + i % C::kQStages), (i / C::kQStages) & 1u, nullptr, kWaitLimitNs);
+            for (uint32_t i = kv_it > C::kStages ? kv_it - C::kStages : 0; i < kv_it; ++i)
+                mbar_wait(bar(BB::kKVFull + i % C::kStages), (i / C::kStages) & 1u, nullptr, kWaitLimitNs);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -647,9 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Every MMA this thread issued is complete before TMEM is released.
+            // Every MMA this thread issued is complete before TMEM is released (bounded by
+            // time only: this wait must not give up early on an abort).
             mma_commit(bar(BB::kMmaDone));
-            mbar_wait(bar(BB::kMmaDone), 0, abort_flag, kWaitLimitNs);
+            mbar_wait(bar(BB::kMmaDone), 0, nullptr, kWaitLimitNs);
         }
     } else if (warp >= 8) {
         setmaxnreg_dec<RegSplit<D>::kControl>(); // idle warps of the control warpgroup
@@ -748,7 +755,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(BB::kPFull + t));
+                // (self-test hook: withholding the first arrival makes the MMA warp's bounded
+                // wait run out; never set in normal use)
+                if (!(p.inject_missing_arrive && j == 0))
+                    mbar_arrive(bar(BB::kPFull + t));
                 ++pv_cnt;
             }
             if (!ok)

@@ -57,8 +57,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete. Every wait is bounded:
-// it gives up (returns false) when `abort` is set by another thread or when
-// `limit_ns` of wall time pass, so a broken handshake can never hang the GPU.
+// it gives up (returns false) when `abort` (if not null) is set by another thread or
+// when `limit_ns` of wall time pass, so a broken handshake can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
                                           uint64_t limit_ns)
 {
@@ -69,7 +69,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
         if (mbar_try_wait(bar, parity))
             return true;
         if ((it & 255u) == 0u) {
-            if (*abort)
+            if (abort && *abort)
                 return false;
             if (globaltimer_ns() - t0 > limit_ns)
                 return false;

@@ -97,6 +97,24 @@ attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o
                             int B, int H, int N, int d, float sm_scale, int causal,
                             const int32_t *key_lengths, int path, attn_stream_t stream);
 
+/* Test hooks of attn_fwd_debug (the pages have no counterpart: these exercise the
+ * library's own bounded waits). */
+typedef struct {
+    uint64_t wait_limit_ns;    /* bound of every on-chip wait; 0 = the default, 4 s */
+    int inject_missing_arrive; /* 1: the softmax warps of the tcgen05 kernel withhold their
+                                  first "P ready" arrival of every unit, so the MMA warp's
+                                  bounded wait runs out and the kernel records
+                                  ATTN_ERR_TIMEOUT (outputs are then undefined); 0 in use */
+} attn_debug_opts_t;
+
+/* attn_fwd_path with test hooks (opts may be NULL = defaults). Used by the self-test of
+ * the timeout path: the launch returns ATTN_OK, and attn_read_device_status() then
+ * reports ATTN_ERR_TIMEOUT while the context stays usable. */
+attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float sm_scale, int causal,
+                             const int32_t *key_lengths, int path, const attn_debug_opts_t *opts,
+                             attn_stream_t stream);
+
 /* The kernel ATTN_PATH_AUTO selects for sequence length N and head dimension d
  * (an attn_path_t value), or -1 when d is unsupported. No CUDA call is made. */
 int attn_auto_path(int N, int d);
