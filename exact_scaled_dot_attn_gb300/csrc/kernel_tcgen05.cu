@@ -107,8 +107,8 @@ constexpr int kMmaWarp = 9;
 // what the CTA launched with (threads x registers per thread); the host checks that
 // 8 * 32 * softmax + 4 * 32 * control fits in it before launching.
 template <int D> struct RegSplit {
-    static constexpr uint32_t kSoftmax = 200;
-    static constexpr uint32_t kControl = D == 128 ? 96 : 72;
+    static constexpr uint32_t kSoftmax = 208;
+    static constexpr uint32_t kControl = D == 128 ? 88 : 72;
     static constexpr int kPoolNeeded = 8 * 32 * kSoftmax + 4 * 32 * kControl;
 };
 constexpr float kLn2 = 0.6931471805599453f;
@@ -122,8 +122,15 @@ template <int D> struct Cfg {
     static constexpr uint32_t kSwizzle = D < 64 ? 4u : 2u; // descriptor layout: 64 B / 128 B swizzle
     static constexpr int kQStages = D == 128 ? 1 : 2;      // Q0/Q1 buffers (2: next unit prefetched)
     static constexpr int kStages = D == 128 ? 5 : (D == 64 ? 9 : 16); // K/V ring depth
-    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
+    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
+    // O accumulators: two per Q tile when they fit (d <= 64), so that a unit's epilogue
+    // can read one while the next unit's PV products accumulate into the other.
+    static constexpr int kOBufs = D <= 64 ? 2 : 1;
     static constexpr uint32_t kTmemCols = 512;
+    __host__ __device__ static constexpr uint32_t tmem_o(int t, int b)
+    {
+        return 256u + static_cast<uint32_t>((b * 2 + t) * D);
+    }
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kQStages * 2 * kTileBytes;
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
@@ -256,9 +263,9 @@ template <int D> struct Bars {
     static constexpr int kKVEmpty = kKVFull + Cfg<D>::kStages;
     static constexpr int kSFull = kKVEmpty + Cfg<D>::kStages; // [2]
     static constexpr int kPFull = kSFull + 2;                 // [2]
-    static constexpr int kOReady = kPFull + 2;                // [2]
-    static constexpr int kOEmpty = kOReady + 2;               // [2]
-    static constexpr int kMmaDone = kOEmpty + 2;
+    static constexpr int kOReady = kPFull + 2;                // [tile * 2 + O buffer]
+    static constexpr int kOEmpty = kOReady + 4;               // [tile * 2 + O buffer]
+    static constexpr int kMmaDone = kOEmpty + 4;
     static constexpr int kCount = kMmaDone + 1;
 };
 
@@ -459,8 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(BB::kSFull + t), 1);
             mbar_init(bar(BB::kPFull + t), kBM);
-            mbar_init(bar(BB::kOReady + t), 1);
-            mbar_init(bar(BB::kOEmpty + t), kBM);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(BB::kOReady + i), 1);
+            mbar_init(bar(BB::kOEmpty + i), kBM);
         }
         mbar_init(bar(BB::kMmaDone), 1);
         *abort_flag = 0;
@@ -538,7 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         setmaxnreg_dec<RegSplit<D>::kControl>();
         if (lane == 0) {
             uint32_t q_it = 0, kv_it = 0;
-            uint32_t p_it[2] = {0, 0}, oe_it[2] = {0, 0};
+            // Phase parities kept as bit masks (no runtime-indexed local arrays):
+            uint32_t p_par = 0;  // bit t: parity of the P-ready waits of tile t
+            uint32_t oe_par = 0; // bit t*2+b: parity of the uses of O buffer b of tile t
+            uint32_t u_par = 0;  // bit t: parity of the units tile t took part in
+            uint32_t ob = 0;     // bit t: O buffer of tile t in the current unit
             bool ok = true;
             auto wait = [&](uint32_t b, uint32_t parity) {
                 if (ok && !mbar_wait(b, parity, abort_flag, kWaitLimitNs)) {
@@ -579,37 +592,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
                 const uint32_t vlo = ((sKV + v_slot * C::kTileBytes) >> 4) | kLboV;
                 const uint32_t a_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
-                const uint32_t d_tmem = tmem + (t ? C::kTmemO1 : C::kTmemO0);
+                const int b = static_cast<int>((ob >> t) & 1u);
+                const uint32_t d_tmem = tmem + C::tmem_o(t, b);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((16 * C::kRowBytes) >> 4)),
                            C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-                mma_commit(bar(BB::kOReady + t));
+                mma_commit(bar(BB::kOReady + t * 2 + b));
             };
             UnitStream us;
             stream_init(us, args, sched);
-            Unit U;
-            while (ok && stream_take(us, args, sched, U)) {
-                if (U.n_kv == 0)
-                    continue;
+            // The next unit that has work (units without an allowed key need no MMA).
+            auto take_work = [&](Unit &X) -> bool {
+                while (stream_take(us, args, sched, X))
+                    if (X.n_kv > 0)
+                        return true;
+                return false;
+            };
+            // A unit's first S products: its Q buffer (q_slot is set to it) and first K tile,
+            // then S_t(0) for every active tile.
+            auto start_unit = [&](const Unit &X) -> bool {
                 q_slot = q_it % C::kQStages;
                 if (!wait(bar(BB::kQFull + q_slot), (q_it / C::kQStages) & 1u))
-                    break;
+                    return false;
                 ++q_it;
-                // prologue: S_t(0) for every active tile
-                uint32_t k_slot = kv_it % C::kStages;
-                if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
-                    break;
+                const uint32_t ks = kv_it % C::kStages;
+                if (!wait(bar(BB::kKVFull + ks), (kv_it / C::kStages) & 1u))
+                    return false;
                 ++kv_it;
                 tc_fence_after();
                 for (int t = 0; t < 2; ++t)
-                    if (kv_tiles(U, t) > 0)
-                        issue_s(t, k_slot);
-                mma_commit(bar(BB::kKVEmpty + k_slot));
-                if (U.n_kv == 1)
+                    if (kv_tiles(X, t) > 0)
+                        issue_s(t, ks);
+                mma_commit(bar(BB::kKVEmpty + ks));
+                if (X.n_kv == 1)
                     mma_commit(bar(BB::kQEmpty + q_slot));
+                return true;
+            };
+            Unit U, Un;
+            bool have = take_work(U);
+            if (have && !start_unit(U))
+                have = false;
+            while (ok && have) {
+                const uint32_t uq_slot = q_slot; // this unit's Q buffer
+                ob = C::kOBufs == 2 ? u_par : 0u;
+                const bool have_next = take_work(Un);
                 // step j: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T; a tile whose
-                // causal range ends earlier drops out of the later steps.
+                // causal range ends earlier drops out of the later steps. After the last
+                // step the next unit's first S products follow at once, so the softmax
+                // warps never wait at a unit boundary for the MMA warp's bookkeeping.
                 for (int j = 0; j < U.n_kv && ok; ++j) {
                     const uint32_t v_slot = kv_it % C::kStages;
                     if (!wait(bar(BB::kKVFull + v_slot), (kv_it / C::kStages) & 1u))
@@ -617,17 +648,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++kv_it;
                     const bool has_next = j + 1 < U.n_kv;
                     bool k_ready = false;
+                    uint32_t k_slot = 0;
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= kv_tiles(U, t))
                             continue;
                         if (j == 0) {
-                            if (!wait(bar(BB::kOEmpty + t), (oe_it[t] & 1u) ^ 1u))
+                            // the epilogue of the last unit that used this O buffer is done
+                            const int ob_i = t * 2 + static_cast<int>((ob >> t) & 1u);
+                            if (!wait(bar(BB::kOEmpty + ob_i), ((oe_par >> ob_i) & 1u) ^ 1u))
                                 break;
-                            ++oe_it[t];
+                            oe_par ^= 1u << ob_i;
                         }
-                        if (!wait(bar(BB::kPFull + t), p_it[t] & 1u))
+                        if (!wait(bar(BB::kPFull + t), (p_par >> t) & 1u))
                             break;
-                        ++p_it[t];
+                        p_par ^= 1u << t;
                         tc_fence_after();
                         issue_pv(t, v_slot, j > 0);
                         if (j + 1 < kv_tiles(U, t)) {
@@ -649,9 +683,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the tile with the most K/V tiles always consumed K_{j+1} above
                         mma_commit(bar(BB::kKVEmpty + k_slot));
                         if (j + 2 == U.n_kv)
-                            mma_commit(bar(BB::kQEmpty + q_slot));
+                            mma_commit(bar(BB::kQEmpty + uq_slot));
+                    } else if (have_next) {
+                        if (!start_unit(Un))
+                            break;
                     }
                 }
+                for (int t = 0; t < 2; ++t)
+                    if (kv_tiles(U, t) > 0)
+                        u_par ^= 1u << t;
+                U = Un;
+                have = have_next;
             }
             // Every MMA this thread issued is complete before TMEM is released (bounded by
             // time only: this wait must not give up early on an abort).
@@ -668,9 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rt = wq * 32 + lane;   // row within the Q tile = TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tS = lane_base + (t ? C::kTmemS1 : C::kTmemS0);
-        const uint32_t tO = lane_base + (t ? C::kTmemO1 : C::kTmemO0);
         const float scale = p.scale_log2;
-        uint32_t s_it = 0, pv_cnt = 0;
+        uint32_t s_it = 0;
+        uint32_t pv_par = 0; // bit b: parity of the PV products committed into O buffer b
+        uint32_t ucnt = 0;   // units in which this tile took part
         bool ok = true;
         // tcgen05.ld/st are warp-collective (.sync.aligned): every branch around them, and
         // every decision to give up, is made uniform across the warp first.
@@ -680,6 +723,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!r)
                 fail();
             return r;
+        };
+        // A unit whose last P has been released but whose epilogue has not run yet. With two
+        // O buffers the epilogue is deferred until the next unit's first P is out, so that
+        // waiting for the last PV product and reading O overlap with the next unit's first
+        // softmax step.
+        struct Pending {
+            bool valid;
+            int bh, row, b;
+            uint32_t last_par; // phase parity of its last PV product in buffer b
+            float l, m_ref;
+        } pend;
+        pend.valid = false;
+        auto finish = [&](const Pending &pe) -> bool {
+            if (!wait_all(bar(BB::kOReady + t * 2 + pe.b), pe.last_par))
+                return false;
+            tc_fence_after();
+            const uint32_t tO = lane_base + C::tmem_o(t, pe.b);
+            const float inv = pe.l > 0.f ? 1.f / pe.l : 0.f;
+            __half *orow = p.o + (static_cast<size_t>(pe.bh) * p.N + pe.row) * D;
+            constexpr int kChunk = D < 64 ? D : 64; // O columns per TMEM load
+#pragma unroll
+            for (int half = 0; half < D / kChunk; ++half) {
+                uint32_t ov[kChunk];
+                if constexpr (kChunk == 64)
+                    tmem_ld64(tO + half * 64, ov);
+                else
+                    tmem_ld32(tO, ov);
+                uint32_t h[kChunk / 2];
+#pragma unroll
+                for (int e = 0; e < kChunk; e += 2)
+                    h[e >> 1] = pack_f16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+                if (pe.row < p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
+#pragma unroll
+                    for (int c = 0; c < kChunk / 8; ++c)
+                        dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(BB::kOEmpty + t * 2 + pe.b));
+            if (p.lse && pe.row < p.N)
+                p.lse[static_cast<size_t>(pe.bh) * p.N + pe.row] =
+                    pe.l > 0.f ? (pe.m_ref + log2f(pe.l)) * kLn2 : -INFINITY;
+            return true;
         };
         UnitStream us;
         stream_init(us, args, sched);
@@ -701,6 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
+            const int b = C::kOBufs == 2 ? static_cast<int>(ucnt & 1u) : 0;
+            const uint32_t tO = lane_base + C::tmem_o(t, b);
             const int row = U.q0 + t * kBM + rt;
             const int tile_row0 = U.q0 + t * kBM;
             float m_ref = -INFINITY; // reference max of the exponentials (log2 units)
@@ -736,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // does it together when any of its rows needs it (tcgen05.ld/st are
                 // warp-collective).
                 if (__any_sync(0xffffffffu, want && l > 0.f)) {
-                    if (!wait_all(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u)) {
+                    if (!wait_all(bar(BB::kOReady + t * 2 + b), ((pv_par >> b) & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
@@ -759,41 +848,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // wait run out; never set in normal use)
                 if (!(p.inject_missing_arrive && j == 0))
                     mbar_arrive(bar(BB::kPFull + t));
-                ++pv_cnt;
+                pv_par ^= 1u << b;
+                // the previous unit's epilogue, now that this unit's first P is out
+                if (j == 0 && pend.valid) {
+                    if (!finish(pend)) {
+                        ok = false;
+                        break;
+                    }
+                    pend.valid = false;
+                }
             }
             if (!ok)
                 break;
-            // epilogue: O / l -> fp16, logsumexp
-            if (!wait_all(bar(BB::kOReady + t), (pv_cnt - 1u) & 1u))
-                break;
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __half *orow = p.o + (static_cast<size_t>(U.bh) * p.N + row) * D;
-            constexpr int kChunk = D < 64 ? D : 64; // O columns per TMEM load
-#pragma unroll
-            for (int half = 0; half < D / kChunk; ++half) {
-                uint32_t ov[kChunk];
-                if constexpr (kChunk == 64)
-                    tmem_ld64(tO + half * 64, ov);
-                else
-                    tmem_ld32(tO, ov);
-                uint32_t h[kChunk / 2];
-#pragma unroll
-                for (int e = 0; e < kChunk; e += 2)
-                    h[e >> 1] = pack_f16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
-                if (row < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
-#pragma unroll
-                    for (int c = 0; c < kChunk / 8; ++c)
-                        dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                }
+            Pending done;
+            done.valid = true;
+            done.bh = U.bh;
+            done.row = row;
+            done.b = b;
+            done.last_par = ((pv_par >> b) & 1u) ^ 1u;
+            done.l = l;
+            done.m_ref = m_ref;
+            ++ucnt;
+            if (C::kOBufs == 1) {
+                // One O buffer: the next unit's PV products wait for this epilogue, so it runs now.
+                if (!finish(done))
+                    break;
+            } else {
+                pend = done;
             }
-            tc_fence_before();
-            mbar_arrive(bar(BB::kOEmpty + t));
-            if (p.lse && row < p.N)
-                p.lse[static_cast<size_t>(U.bh) * p.N + row] =
-                    l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         }
+        if (ok && pend.valid)
+            finish(pend);
     }
 
     tc_fence_before();

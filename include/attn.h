@@ -61,9 +61,8 @@ typedef enum {
     ATTN_ERR_TIMEOUT = 5      /* a bounded on-chip wait ran out (see attn_read_device_status) */
 } attn_status_t;
 
-/* Which kernel runs the forward. AUTO picks by shape: the short-sequence kernel
- * for N <= 256 with d in {32, 64}; the tcgen05 kernel for d = 128, and for d = 64
- * with N > 256; the warp-level kernel for d = 32 with N > 256. */
+/* Which kernel runs the forward. AUTO runs the tcgen05 kernel (the fastest at every
+ * measured shape); the warp-level kernels remain selectable explicitly. */
 typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_WARP_MMA = 1, /* warp-level mma.sync tile kernel: every d, every N */
