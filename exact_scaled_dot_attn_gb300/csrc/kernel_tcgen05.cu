@@ -454,6 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const FwdParams &p = args.p;
     const uint64_t kWaitLimitNs = p.wait_limit_ns;
 
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kQStages; ++s) {
             mbar_init(bar(BB::kQFull + s), 1);
@@ -490,216 +495,241 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
 
+    // Bounded wait of a whole warp; the outcome is made warp-uniform.
+    auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
+        bool r = mbar_wait(b, parity, abort_flag, kWaitLimitNs);
+        r = __all_sync(0xffffffffu, r);
+        if (!r && lane == 0)
+            fail();
+        return r;
+    };
+
+    // The producer and MMA roles run on whole warps (converged control flow, warp-uniform
+    // operands); one elected lane issues each TMA copy, tcgen05.mma and commit.
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         setmaxnreg_dec<RegSplit<D>::kControl>();
-        if (lane == 0) {
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            uint32_t q_it = 0, kv_it = 0;
-            bool ok = true;
-            UnitStream us;
-            stream_init(us, args, sched);
-            Unit U;
-            while (ok && stream_take(us, args, sched, U)) {
-                if (U.n_kv == 0)
-                    continue;
-                const uint32_t qs = q_it % C::kQStages;
-                if (!mbar_wait(bar(BB::kQEmpty + qs), ((q_it / C::kQStages) & 1u) ^ 1u, abort_flag,
-                               kWaitLimitNs)) {
-                    fail();
-                    break;
-                }
-                ++q_it;
+        uint32_t q_it = 0, kv_it = 0;
+        bool ok = true;
+        UnitStream us;
+        stream_init(us, args, sched);
+        Unit U;
+        while (ok && stream_take(us, args, sched, U)) {
+            if (U.n_kv == 0)
+                continue;
+            const uint32_t qs = q_it % C::kQStages;
+            if (!warp_wait(bar(BB::kQEmpty + qs), ((q_it / C::kQStages) & 1u) ^ 1u))
+                break;
+            ++q_it;
+            if (elect_one()) {
                 mbar_arrive_expect_tx(bar(BB::kQFull + qs), 2 * C::kTileBytes);
+#pragma unroll
                 for (int t = 0; t < 2; ++t)
+#pragma unroll
                     for (int bx = 0; bx < D / C::kBoxCols; ++bx)
                         tma_load_3d(sQ + (qs * 2 + t) * C::kTileBytes + bx * C::kBoxBytes, &tm_q,
                                     bar(BB::kQFull + qs), bx * C::kBoxCols, U.q0 + t * kBM, U.bh);
-                for (int j = 0; j < U.n_kv && ok; ++j) {
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint32_t slot = kv_it % C::kStages;
-                        const uint32_t ph = (kv_it / C::kStages) & 1u;
-                        if (!mbar_wait(bar(BB::kKVEmpty + slot), ph ^ 1u, abort_flag, kWaitLimitNs)) {
-                            fail();
-                            ok = false;
-                            break;
-                        }
+            }
+            __syncwarp();
+            for (int j = 0; j < U.n_kv && ok; ++j) {
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t slot = kv_it % C::kStages;
+                    const uint32_t ph = (kv_it / C::kStages) & 1u;
+                    if (!warp_wait(bar(BB::kKVEmpty + slot), ph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) {
                         mbar_arrive_expect_tx(bar(BB::kKVFull + slot), C::kTileBytes);
+#pragma unroll
                         for (int bx = 0; bx < D / C::kBoxCols; ++bx)
                             tma_load_3d(sKV + slot * C::kTileBytes + bx * C::kBoxBytes,
                                         kv == 0 ? &tm_k : &tm_v, bar(BB::kKVFull + slot),
                                         bx * C::kBoxCols, j * kBN, U.bh);
-                        ++kv_it;
                     }
+                    __syncwarp();
+                    ++kv_it;
                 }
             }
-            // Loads still in flight land before the CTA may leave (after an abort): wait,
-            // bounded by time only, for the latest phase of every slot that was filled.
+        }
+        // Loads still in flight land before the CTA may leave (after an abort): wait,
+        // bounded by time only, for the latest phase of every slot that was filled.
+        if (lane == 0) {
             for (uint32_t i = q_it > C::kQStages ? q_it - C::kQStages : 0; i < q_it; ++i)
                 mbar_wait(bar(BB::kQFull + i % C::kQStages), (i / C::kQStages) & 1u, nullptr, kWaitLimitNs);
             for (uint32_t i = kv_it > C::kStages ? kv_it - C::kStages : 0; i < kv_it; ++i)
                 mbar_wait(bar(BB::kKVFull + i % C::kStages), (i / C::kStages) & 1u, nullptr, kWaitLimitNs);
         }
+        __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         setmaxnreg_dec<RegSplit<D>::kControl>();
-        if (lane == 0) {
-            uint32_t q_it = 0, kv_it = 0;
-            // Phase parities kept as bit masks (no runtime-indexed local arrays):
-            uint32_t p_par = 0;  // bit t: parity of the P-ready waits of tile t
-            uint32_t oe_par = 0; // bit t*2+b: parity of the uses of O buffer b of tile t
-            uint32_t u_par = 0;  // bit t: parity of the units tile t took part in
-            uint32_t ob = 0;     // bit t: O buffer of tile t in the current unit
-            bool ok = true;
-            auto wait = [&](uint32_t b, uint32_t parity) {
-                if (ok && !mbar_wait(b, parity, abort_flag, kWaitLimitNs)) {
-                    fail();
-                    ok = false;
-                }
-                return ok;
-            };
-            uint32_t q_slot = 0;
-            // Shared-memory descriptors, built once: the high word (stride byte offset,
-            // version, swizzle layout) is the same for every operand; the low word is
-            // (start address >> 4) | (leading byte offset >> 4) << 16, so stepping through
-            // a tile is one add per instruction. Addresses stay below 2^18, so the start
-            // field never carries into the leading-offset field.
-            constexpr uint32_t kDescHi = ((8 * C::kRowBytes) >> 4) | (1u << 14) | (C::kSwizzle << 29);
-            constexpr uint32_t kLboK = (16u >> 4) << 16;                            // K-major: unused
-            constexpr uint32_t kLboV = (static_cast<uint32_t>(C::kBoxBytes) >> 4) << 16; // next 64 columns of d
-            auto desc = [](uint32_t lo) -> uint64_t {
-                return (static_cast<uint64_t>(kDescHi) << 32) | lo;
-            };
-            // S_t = Q_t K^T: K-major operands, 16 columns (32 bytes) per k-step inside a
-            // swizzle row, a new box every kBoxCols / 16 steps.
-            auto issue_s = [&](int t, uint32_t k_slot) {
-                const uint32_t qlo = ((sQ + (q_slot * 2 + t) * C::kTileBytes) >> 4) | kLboK;
-                const uint32_t klo = ((sKV + k_slot * C::kTileBytes) >> 4) | kLboK;
-                const uint32_t d_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
-                constexpr int kStepsPerBox = C::kBoxCols / 16;
+        uint32_t q_it = 0, kv_it = 0;
+        // Phase parities kept as bit masks (no runtime-indexed local arrays):
+        uint32_t p_par = 0;  // bit t: parity of the P-ready waits of tile t
+        uint32_t oe_par = 0; // bit t*2+b: parity of the uses of O buffer b of tile t
+        uint32_t u_par = 0;  // bit t: parity of the units tile t took part in
+        uint32_t ob = 0;     // bit t: O buffer of tile t in the current unit
+        bool ok = true;
+        auto wait = [&](uint32_t b, uint32_t parity) {
+            if (ok && !warp_wait(b, parity))
+                ok = false;
+            return ok;
+        };
+        uint32_t q_slot = 0;
+        // Shared-memory descriptors, built once: the high word (stride byte offset,
+        // version, swizzle layout) is the same for every operand; the low word is
+        // (start address >> 4) | (leading byte offset >> 4) << 16, so stepping through
+        // a tile is one add per instruction. Addresses stay below 2^18, so the start
+        // field never carries into the leading-offset field.
+        constexpr uint32_t kDescHi = ((8 * C::kRowBytes) >> 4) | (1u << 14) | (C::kSwizzle << 29);
+        constexpr uint32_t kLboK = (16u >> 4) << 16;                            // K-major: unused
+        constexpr uint32_t kLboV = (static_cast<uint32_t>(C::kBoxBytes) >> 4) << 16; // next 64 columns of d
+        auto desc = [](uint32_t lo) -> uint64_t {
+            return (static_cast<uint64_t>(kDescHi) << 32) | lo;
+        };
+        // S_t = Q_t K^T: K-major operands, 16 columns (32 bytes) per k-step inside a
+        // swizzle row, a new box every kBoxCols / 16 steps. (Issued by the elected lane.)
+        auto issue_s = [&](int t, uint32_t k_slot) {
+            const uint32_t qlo = ((sQ + (q_slot * 2 + t) * C::kTileBytes) >> 4) | kLboK;
+            const uint32_t klo = ((sKV + k_slot * C::kTileBytes) >> 4) | kLboK;
+            const uint32_t d_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
+            constexpr int kStepsPerBox = C::kBoxCols / 16;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    constexpr int kBox16 = C::kBoxBytes >> 4;
-                    const uint32_t off = (kk / kStepsPerBox) * kBox16 + (kk % kStepsPerBox) * 2;
-                    mma_ss(d_tmem, desc(qlo + off), desc(klo + off), C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(bar(BB::kSFull + t));
-            };
-            // O_t += P_t V: P from TMEM (8 columns = 16 fp16 keys per k-step); V is MN-major,
-            // 16 keys (rows) per k-step.
-            auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
-                const uint32_t vlo = ((sKV + v_slot * C::kTileBytes) >> 4) | kLboV;
-                const uint32_t a_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
-                const int b = static_cast<int>((ob >> t) & 1u);
-                const uint32_t d_tmem = tmem + C::tmem_o(t, b);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                constexpr int kBox16 = C::kBoxBytes >> 4;
+                const uint32_t off = (kk / kStepsPerBox) * kBox16 + (kk % kStepsPerBox) * 2;
+                mma_ss(d_tmem, desc(qlo + off), desc(klo + off), C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar(BB::kSFull + t));
+        };
+        // O_t += P_t V: P from TMEM (8 columns = 16 fp16 keys per k-step); V is MN-major,
+        // 16 keys (rows) per k-step. (Issued by the elected lane.)
+        auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
+            const uint32_t vlo = ((sKV + v_slot * C::kTileBytes) >> 4) | kLboV;
+            const uint32_t a_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
+            const int b = static_cast<int>((ob >> t) & 1u);
+            const uint32_t d_tmem = tmem + C::tmem_o(t, b);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((16 * C::kRowBytes) >> 4)),
-                           C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-                mma_commit(bar(BB::kOReady + t * 2 + b));
-            };
-            UnitStream us;
-            stream_init(us, args, sched);
-            // The next unit that has work (units without an allowed key need no MMA).
-            auto take_work = [&](Unit &X) -> bool {
-                while (stream_take(us, args, sched, X))
-                    if (X.n_kv > 0)
-                        return true;
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((16 * C::kRowBytes) >> 4)),
+                       C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            mma_commit(bar(BB::kOReady + t * 2 + b));
+        };
+        UnitStream us;
+        stream_init(us, args, sched);
+        // The next unit that has work (units without an allowed key need no MMA).
+        auto take_work = [&](Unit &X) -> bool {
+            while (stream_take(us, args, sched, X))
+                if (X.n_kv > 0)
+                    return true;
+            return false;
+        };
+        // A unit's first S products: its Q buffer (q_slot is set to it) and first K tile,
+        // then S_t(0) for every active tile.
+        auto start_unit = [&](const Unit &X) -> bool {
+            q_slot = q_it % C::kQStages;
+            if (!wait(bar(BB::kQFull + q_slot), (q_it / C::kQStages) & 1u))
                 return false;
-            };
-            // A unit's first S products: its Q buffer (q_slot is set to it) and first K tile,
-            // then S_t(0) for every active tile.
-            auto start_unit = [&](const Unit &X) -> bool {
-                q_slot = q_it % C::kQStages;
-                if (!wait(bar(BB::kQFull + q_slot), (q_it / C::kQStages) & 1u))
-                    return false;
-                ++q_it;
-                const uint32_t ks = kv_it % C::kStages;
-                if (!wait(bar(BB::kKVFull + ks), (kv_it / C::kStages) & 1u))
-                    return false;
-                ++kv_it;
-                tc_fence_after();
+            ++q_it;
+            const uint32_t ks = kv_it % C::kStages;
+            if (!wait(bar(BB::kKVFull + ks), (kv_it / C::kStages) & 1u))
+                return false;
+            ++kv_it;
+            tc_fence_after();
+            if (elect_one()) {
                 for (int t = 0; t < 2; ++t)
                     if (kv_tiles(X, t) > 0)
                         issue_s(t, ks);
                 mma_commit(bar(BB::kKVEmpty + ks));
                 if (X.n_kv == 1)
                     mma_commit(bar(BB::kQEmpty + q_slot));
-                return true;
-            };
-            Unit U, Un;
-            bool have = take_work(U);
-            if (have && !start_unit(U))
-                have = false;
-            while (ok && have) {
-                const uint32_t uq_slot = q_slot; // this unit's Q buffer
-                ob = C::kOBufs == 2 ? u_par : 0u;
-                const bool have_next = take_work(Un);
-                // step j: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T; a tile whose
-                // causal range ends earlier drops out of the later steps. After the last
-                // step the next unit's first S products follow at once, so the softmax
-                // warps never wait at a unit boundary for the MMA warp's bookkeeping.
-                for (int j = 0; j < U.n_kv && ok; ++j) {
-                    const uint32_t v_slot = kv_it % C::kStages;
-                    if (!wait(bar(BB::kKVFull + v_slot), (kv_it / C::kStages) & 1u))
-                        break;
-                    ++kv_it;
-                    const bool has_next = j + 1 < U.n_kv;
-                    bool k_ready = false;
-                    uint32_t k_slot = 0;
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (j >= kv_tiles(U, t))
-                            continue;
-                        if (j == 0) {
-                            // the epilogue of the last unit that used this O buffer is done
-                            const int ob_i = t * 2 + static_cast<int>((ob >> t) & 1u);
-                            if (!wait(bar(BB::kOEmpty + ob_i), ((oe_par >> ob_i) & 1u) ^ 1u))
-                                break;
-                            oe_par ^= 1u << ob_i;
-                        }
-                        if (!wait(bar(BB::kPFull + t), (p_par >> t) & 1u))
+            }
+            __syncwarp();
+            return true;
+        };
+        Unit U, Un;
+        bool have = take_work(U);
+        if (have && !start_unit(U))
+            have = false;
+        while (ok && have) {
+            const uint32_t uq_slot = q_slot; // this unit's Q buffer
+            ob = C::kOBufs == 2 ? u_par : 0u;
+            const bool have_next = take_work(Un);
+            // step j: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T; a tile whose
+            // causal range ends earlier drops out of the later steps. After the last
+            // step the next unit's first S products follow at once, so the softmax
+            // warps never wait at a unit boundary for the MMA warp's bookkeeping.
+            for (int j = 0; j < U.n_kv && ok; ++j) {
+                const uint32_t v_slot = kv_it % C::kStages;
+                if (!wait(bar(BB::kKVFull + v_slot), (kv_it / C::kStages) & 1u))
+                    break;
+                ++kv_it;
+                const bool has_next = j + 1 < U.n_kv;
+                bool k_ready = false;
+                uint32_t k_slot = 0;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= kv_tiles(U, t))
+                        continue;
+                    if (j == 0) {
+                        // the epilogue of the last unit that used this O buffer is done
+                        const int ob_i = t * 2 + static_cast<int>((ob >> t) & 1u);
+                        if (!wait(bar(BB::kOEmpty + ob_i), ((oe_par >> ob_i) & 1u) ^ 1u))
                             break;
-                        p_par ^= 1u << t;
-                        tc_fence_after();
-                        issue_pv(t, v_slot, j > 0);
-                        if (j + 1 < kv_tiles(U, t)) {
-                            if (!k_ready) {
-                                k_slot = kv_it % C::kStages;
-                                if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
-                                    break;
-                                ++kv_it;
-                                k_ready = true;
-                                tc_fence_after();
-                            }
-                            issue_s(t, k_slot);
-                        }
+                        oe_par ^= 1u << ob_i;
                     }
-                    if (!ok)
+                    if (!wait(bar(BB::kPFull + t), (p_par >> t) & 1u))
                         break;
+                    p_par ^= 1u << t;
+                    tc_fence_after();
+                    if (elect_one())
+                        issue_pv(t, v_slot, j > 0);
+                    __syncwarp();
+                    if (j + 1 < kv_tiles(U, t)) {
+                        if (!k_ready) {
+                            k_slot = kv_it % C::kStages;
+                            if (!wait(bar(BB::kKVFull + k_slot), (kv_it / C::kStages) & 1u))
+                                break;
+                            ++kv_it;
+                            k_ready = true;
+                            tc_fence_after();
+                        }
+                        if (elect_one())
+                            issue_s(t, k_slot);
+                        __syncwarp();
+                    }
+                }
+                if (!ok)
+                    break;
+                if (elect_one()) {
                     mma_commit(bar(BB::kKVEmpty + v_slot));
                     if (has_next) {
                         // the tile with the most K/V tiles always consumed K_{j+1} above
                         mma_commit(bar(BB::kKVEmpty + k_slot));
                         if (j + 2 == U.n_kv)
                             mma_commit(bar(BB::kQEmpty + uq_slot));
-                    } else if (have_next) {
-                        if (!start_unit(Un))
-                            break;
                     }
                 }
-                for (int t = 0; t < 2; ++t)
-                    if (kv_tiles(U, t) > 0)
-                        u_par ^= 1u << t;
-                U = Un;
-                have = have_next;
+                __syncwarp();
+                if (!has_next && have_next) {
+                    if (!start_unit(Un))
+                        break;
+                }
             }
-            // Every MMA this thread issued is complete before TMEM is released (bounded by
-            // time only: this wait must not give up early on an abort).
-            mma_commit(bar(BB::kMmaDone));
-            mbar_wait(bar(BB::kMmaDone), 0, nullptr, kWaitLimitNs);
+            for (int t = 0; t < 2; ++t)
+                if (kv_tiles(U, t) > 0)
+                    u_par ^= 1u << t;
+            U = Un;
+            have = have_next;
         }
+        // Every MMA this warp issued is complete before TMEM is released (bounded by
+        // time only: this wait must not give up early on an abort).
+        if (elect_one())
+            mma_commit(bar(BB::kMmaDone));
+        __syncwarp();
+        mbar_wait(bar(BB::kMmaDone), 0, nullptr, kWaitLimitNs);
+        __syncwarp();
     } else if (warp >= 8) {
         setmaxnreg_dec<RegSplit<D>::kControl>(); // idle warps of the control warpgroup
     } else {

@@ -44,14 +44,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Tests the phase with the given parity; a thread whose phase is not complete yet is
+// suspended (up to kSuspendHintNs) instead of spinning, so waiting warps leave the issue
+// slots to the warps that compute.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}\n"
                  : "=r"(ok)
-                 : "r"(bar), "r"(parity)
+                 : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
                  : "memory");
     return ok != 0;
 }
@@ -68,13 +72,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((it & 255u) == 0u) {
+        if ((it & 15u) == 0u) {
             if (abort && *abort)
                 return false;
             if (globaltimer_ns() - t0 > limit_ns)
                 return false;
         }
     }
+}
+
+// One lane of the (converged) warp is elected: the lane that issues a single-thread
+// operation (tcgen05.mma, commit, TMA) while the whole warp runs the role's control flow.
+// Operands computed by the whole warp stay warp-uniform, which keeps the issue of a
+// tcgen05.mma down to a few cycles (a single-lane branch around the role makes every
+// operand per-thread and the issue several times slower).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+                 "elect.sync r|p, 0xffffffff;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(pred));
+    return pred != 0;
 }
 
 // ------------------------------------------------------------------ TMA
