@@ -359,29 +359,68 @@ def main():
 
 
 def short_n(torch, api, peaks, peak_src):
-    """Reranking workload in GB/s of minimum traffic, L2 flushed before each timed launch."""
+    """Reranking workload in GB/s of minimum traffic (Q, K, V, O once at full padded size).
+
+    Inputs larger than L2: the launches rotate over buffer sets whose total is more than
+    twice the L2 size, so every launch reads its inputs from HBM. The launches run back to
+    back from a CUDA graph (as a serving loop would issue them), timed with CUDA events
+    around the replays; the per-launch time is the total over the launch count. A single
+    launch right after a 512 MiB write (L2 flushed, launch latency included) is reported
+    beside it.
+    """
+    import math
     w = synth.WORKLOADS["rerank"]
     q, k, v, kl = synth.draw_workload(w)
-    qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
-    kld = torch.from_numpy(kl).cuda()
-    od = torch.empty_like(qd)
+    nbytes = synth.min_bytes(w.B, w.H, w.N, w.d) + kl.nbytes
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    nsets = max(2, math.ceil(2 * l2 / nbytes) + 1)
+    sets = []
+    for _ in range(nsets):
+        qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+        sets.append((qd, kd, vd, torch.from_numpy(kl).cuda(), torch.empty_like(qd)))
 
-    def fn():
+    def fn(i):
+        qd, kd, vd, kld, od = sets[i % nsets]
         api.fwd(qd, kd, vd, causal=False, sm_scale=w.sm_scale, key_lengths=kld, out=od)
 
+    for i in range(2 * nsets):
+        fn(i)
+    torch.cuda.synchronize()
+    per_graph = 4 * nsets
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(per_graph):
+                fn(i)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 10
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    launch_ms = a.elapsed_time(b) / (reps * per_graph)
+    gbs = nbytes / (launch_ms * 1e-3) / 1e9
     flush = l2_flush_buffer(torch)
-    time_launches(torch, fn, 5, flush)
-    ms = time_launches(torch, fn, 50, flush)
-    med = statistics.median(ms)
-    nbytes = synth.min_bytes(w.B, w.H, w.N, w.d) + kl.nbytes
-    gbs = nbytes / (med * 1e-3) / 1e9
+    time_launches(torch, lambda: fn(0), 3, flush)
+    flushed_ms = statistics.median(time_launches(torch, lambda: fn(0), 30, flush))
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     valid_bytes = int(sum(int(L) for L in kl) * w.H * w.d * 2 * 2 + q.nbytes * 2)
-    return {"workload": w.describe(), "value": gbs, "unit": "GB/s", "median_launch_ms": med,
-            "bytes": nbytes, "valid_only_bytes": valid_bytes,
+    kernel = api.auto_path(w.N, w.d)
+    return {"workload": w.describe(), "value": gbs, "unit": "GB/s", "launch_ms": launch_ms,
+            "bytes": nbytes, "valid_only_bytes": valid_bytes, "kernel": kernel,
+            "gpu_launches": reps * per_graph,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_source": f"{peak_src} copy bandwidth"},
-            "l2": "flushed (512 MiB write) before every timed launch"}
+            "l2": f"inputs larger than L2: {nsets} rotating buffer sets ({nsets * nbytes / 1e6:.0f} MB)",
+            "flushed_single_launch": {"ms": flushed_ms,
+                                      "value": nbytes / (flushed_ms * 1e-3) / 1e9, "unit": "GB/s",
+                                      "l2": "flushed (512 MiB write) before the launch"}}
 
 
 if __name__ == "__main__":

@@ -84,7 +84,10 @@ extern "C" int attn_auto_path(int N, int d)
 {
     if (d != 32 && d != 64 && d != 128)
         return -1;
-    (void)N; // the tcgen05 kernel is the fastest path at every measured length
+    // Head dimension 32 with at most 256 keys: the short-sequence kernel (a whole score row
+    // per Q tile in Tensor Memory); everything else: the tiled tcgen05 kernel.
+    if (d == 32 && N <= 256)
+        return ATTN_PATH_SHORT;
     return ATTN_PATH_TCGEN05;
 }
 

@@ -59,8 +59,8 @@ template <int D> struct SCfg {
     static constexpr uint32_t kTmemO = kTmemCols - D;       // first column of the O accumulator
     static constexpr int kOffBar = kSlots * kSlotBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kOffSort = kOffBar + kBarBytes;    // key lengths and their sorted order
-    static constexpr int kSmemBytes = kOffSort + 2 * kMaxSortB * 4 + 1024; // + alignment slack
+    static constexpr int kOffSort = kOffBar + kBarBytes;    // key lengths, sorted order, sort keys
+    static constexpr int kSmemBytes = kOffSort + 3 * kMaxSortB * 4 + 1024; // + alignment slack
     static constexpr uint32_t kIdescPV = idesc_f16_f32(kBM, D, 0, 1);
 };
 
@@ -201,9 +201,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
+    // Sort keys: (length << 16) | (0xffff - index), so that "greater" means longer, or as
+    // long with a smaller index. Padded to a multiple of 4 with keys smaller than any real one.
+    int *s_key = s_inv + kMaxSortB;
     if (args.sorted)
-        for (int b = threadIdx.x; b < p.B; b += kThreads)
-            s_len[b] = clamp_len(__ldg(p.key_lengths + b), N);
+        for (int b = threadIdx.x; b < ((p.B + 3) & ~3); b += kThreads) {
+            const int Lb = b < p.B ? clamp_len(__ldg(p.key_lengths + b), N) : -1;
+            if (b < p.B)
+                s_len[b] = Lb;
+            s_key[b] = Lb < 0 ? -1 : ((Lb << 16) | (0xffff - b));
+        }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kSlots; ++s) {
             mbar_init(bar(BB::kQKFull + s), 1);
@@ -225,12 +232,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     // The longest-first order of the batches (rank by key length, then by index).
     if (args.sorted) {
         __syncthreads();
+        const int4 *keys4 = reinterpret_cast<const int4 *>(s_key);
+        const int n4 = (p.B + 3) >> 2;
         for (int b = threadIdx.x; b < p.B; b += kThreads) {
-            const int Lb = s_len[b];
+            const int kb = s_key[b];
             int rank = 0;
-            for (int o = 0; o < p.B; ++o) {
-                const int Lo = s_len[o];
-                rank += (Lo > Lb) || (Lo == Lb && o < b);
+            for (int o = 0; o < n4; ++o) {
+                const int4 q = keys4[o];
+                rank += (q.x > kb) + (q.y > kb) + (q.z > kb) + (q.w > kb);
             }
             s_inv[rank] = b;
         }

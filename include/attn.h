@@ -61,13 +61,16 @@ typedef enum {
     ATTN_ERR_TIMEOUT = 5      /* a bounded on-chip wait ran out (see attn_read_device_status) */
 } attn_status_t;
 
-/* Which kernel runs the forward. AUTO runs the tcgen05 kernel (the fastest at every
- * measured shape); the warp-level kernels remain selectable explicitly. */
+/* Which kernel runs the forward. AUTO runs the short-sequence kernel for d = 32 with
+ * N <= 256 and the tiled tcgen05 kernel everywhere else (the fastest at every measured
+ * shape); the other kernels remain selectable explicitly. */
 typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_WARP_MMA = 1, /* warp-level mma.sync tile kernel: every d, every N */
-    ATTN_PATH_TCGEN05 = 2,  /* TMA + tcgen05/TMEM warp-specialised kernel: every d, every N */
-    ATTN_PATH_SHORT = 3     /* persistent whole-head kernel: N <= 256, d in {32, 64} */
+    ATTN_PATH_TCGEN05 = 2,  /* TMA + tcgen05/TMEM warp-specialised tiled kernel: every d, every N */
+    ATTN_PATH_SHORT = 3     /* tcgen05 kernel holding a Q tile's whole score row in TMEM
+                               (two CTAs per SM, heads dealt longest first): N <= 256,
+                               d in {32, 64} */
 } attn_path_t;
 
 /*
