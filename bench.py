@@ -185,8 +185,21 @@ def workload_config(w):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def source_digest(files):
+    """First 16 hex digits of the sha256 of the listed source files, concatenated."""
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profile(kernel_name: str, workload: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it still matches the source."""
+    """Per-launch DRAM bytes from the committed ncu summary, if it still matches the source.
+
+    profiles/<kernel>_<workload>_traffic.txt records the DRAM read + write bytes of one launch
+    and a digest of the kernel's source files; a kernel changed since the capture gives None.
+    """
     path = os.path.join(ROOT, "profiles", f"{kernel_name}_{workload}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -195,11 +208,10 @@ def traffic_from_profile(kernel_name: str, workload: str):
         if ":" in line and not line.startswith("#"):
             key, val = line.split(":", 1)
             vals[key.strip()] = val.strip()
-    src = vals.get("source_file")
-    if not src or not os.path.exists(os.path.join(ROOT, src)):
+    files = [f.strip() for f in vals.get("source_files", "").split(",") if f.strip()]
+    if not files or not all(os.path.exists(os.path.join(ROOT, f)) for f in files):
         return None
-    digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
-    if digest != vals.get("source_sha256_16"):
+    if source_digest(files) != vals.get("source_sha256_16"):
         return None  # the kernel changed since the counters were taken
     try:
         return float(vals["traffic_bytes_per_launch"])
@@ -416,7 +428,8 @@ def short_n(torch, api, peaks, peak_src):
             "bytes": nbytes, "valid_only_bytes": valid_bytes, "kernel": kernel,
             "gpu_launches": reps * per_graph,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                         "frac": gbs / peak, "peak_source": f"{peak_src} copy bandwidth"},
+                         "frac": gbs / peak, "peak_source": f"{peak_src} copy bandwidth",
+                         "traffic": traffic_from_profile(kernel, "rerank")},
             "l2": f"inputs larger than L2: {nsets} rotating buffer sets ({nsets * nbytes / 1e6:.0f} MB)",
             "flushed_single_launch": {"ms": flushed_ms,
                                       "value": nbytes / (flushed_ms * 1e-3) / 1e9, "unit": "GB/s",
