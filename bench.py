@@ -59,6 +59,27 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of `value` over all ranks (the value itself in a single process).
+
+    With one process per GPU the slowest rank sets the time of a step; the collective is
+    only for timing, never on the data path.
+    """
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world: int, work_per_rank: float, seconds: float, unit_scale: float = 1e12):
+    """Whole-job throughput: every rank processes its own copy of the workload, so the
+    work of all ranks is divided by the slowest rank's time."""
+    return world * work_per_rank / seconds / unit_scale
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -297,12 +318,9 @@ def main():
     clocks = sampler.stop()
     region_ms = evs[0][0].elapsed_time(evs[-1][1])
     launch_ms = [a.elapsed_time(b) for a, b in evs]
-    if world > 1:
-        t = torch.tensor([region_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(region_ms, device="cuda")
     ms_per_step = region_ms / steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = weak_scaling_value(world, flops, ms_per_step * 1e-3)
 
     # End to end through the public API with host tensors.
     e2e_steps = max(1, min(args.e2e_steps, steps))
@@ -320,11 +338,7 @@ def main():
         api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
                 path=args.path)
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, device="cuda")
     h2d = sum(x.nbytes for x in (q, k, v)) + (kl.nbytes if kl is not None else 0)
     d2h = q.nbytes
 
@@ -343,7 +357,7 @@ def main():
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": dict(workload_config(w), path=args.path, kernel=kernel_name),
-        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": weak_scaling_value(world, flops, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": steps,
         "roofline": roofline,
