@@ -195,22 +195,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n_qt = (N + kBM - 1) / kBM; // Q tiles per head (1 or 2)
     const uint64_t kWaitLimitNs = p.wait_limit_ns;
 
-    // The descriptors and key lengths are fetched first, so their latency overlaps the setup.
+    // Setup that reads no input overlaps the end of the previous kernel of the stream
+    // (programmatic dependent launch); inputs are read only after griddep_wait.
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
-    // Sort keys: (length << 16) | (0xffff - index), so that "greater" means longer, or as
-    // long with a smaller index. Padded to a multiple of 4 with keys smaller than any real one.
-    int *s_key = s_inv + kMaxSortB;
-    if (args.sorted)
-        for (int b = threadIdx.x; b < ((p.B + 3) & ~3); b += kThreads) {
-            const int Lb = b < p.B ? clamp_len(__ldg(p.key_lengths + b), N) : -1;
-            if (b < p.B)
-                s_len[b] = Lb;
-            s_key[b] = Lb < 0 ? -1 : ((Lb << 16) | (0xffff - b));
-        }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kSlots; ++s) {
             mbar_init(bar(BB::kQKFull + s), 1);
@@ -229,6 +220,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    griddep_launch_dependents();
+    griddep_wait();
+    // Sort keys: (length << 16) | (0xffff - index), so that "greater" means longer, or as
+    // long with a smaller index. Padded to a multiple of 4 with keys smaller than any real one.
+    int *s_key = s_inv + kMaxSortB;
+    if (args.sorted)
+        for (int b = threadIdx.x; b < ((p.B + 3) & ~3); b += kThreads) {
+            const int Lb = b < p.B ? clamp_len(__ldg(p.key_lengths + b), N) : -1;
+            if (b < p.B)
+                s_len[b] = Lb;
+            s_key[b] = Lb < 0 ? -1 : ((Lb << 16) | (0xffff - b));
+        }
     // The longest-first order of the batches (rank by key length, then by index).
     if (args.sorted) {
         __syncthreads();
@@ -606,8 +609,19 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     a.sorted = (p.key_lengths != nullptr && p.B <= kMaxSortB) ? 1 : 0;
     a.status = status;
     const int grid = BH < 2 * sms ? BH : 2 * sms;
-    attn_fwd_short_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv);
-    return cudaGetLastError();
+    // Programmatic dependent launch: this kernel's setup may overlap the previous kernel of
+    // the stream (the kernel waits for it before reading any input).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_fwd_short_kernel<D>, a, mq, mk, mv);
 }
 
 } // namespace

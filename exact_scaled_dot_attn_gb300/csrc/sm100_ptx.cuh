@@ -96,6 +96,12 @@ __device__ __forceinline__ bool elect_one()
     return pred != 0;
 }
 
+// Programmatic dependent launch: the next kernel of the stream may start its prologue
+// (launch_dependents), and this grid waits for the previous one to complete and its memory
+// to be visible before it reads anything that kernel may have written (wait).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 // 3-D tiled load into shared memory; completion is reported to `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
