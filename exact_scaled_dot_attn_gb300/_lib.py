@@ -39,6 +39,10 @@ SIGNATURES = {
     "attn_auto_path": (_i, [_i, _i]),
     "attn_status_str": (ctypes.c_char_p, [_i]),
     "attn_read_device_status": (_i, [_vp]),
+    "attn_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp,
+                              ctypes.c_size_t, _vp]),
+    "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
+    "attn_splitkv_auto_splits": (_i, [_i, _i, _i, _i]),
 }
 
 _lib = None

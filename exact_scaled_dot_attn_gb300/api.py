@@ -79,6 +79,63 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
     return (out, lse) if return_lse else out
 
 
+def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+                sm_scale: float | None = None, key_lengths: torch.Tensor | None = None,
+                return_lse: bool = False, out: torch.Tensor | None = None,
+                lse_out: torch.Tensor | None = None, n_splits: int = 0,
+                workspace: torch.Tensor | None = None):
+    """fwd() with the keys of every query tile pair split into n_splits ranges that run as
+    separate work units and are merged exactly (attn_fwd_splitkv). n_splits <= 0 chooses the
+    count for the current device. workspace: a CUDA tensor of at least
+    splitkv_workspace_bytes(...) bytes (allocated here when None). Device tensors only."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("fwd_splitkv takes CUDA tensors")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_device_tensor(name, t, (B, H, N, d), torch.float16, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_device_tensor("out", out, (B, H, N, d), torch.float16, dev)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, H, N), device=dev,
+                                                               dtype=torch.float32)
+        _check_device_tensor("lse_out", lse, (B, H, N), torch.float32, dev)
+    if key_lengths is not None:
+        _check_device_tensor("key_lengths", key_lengths, (B,), torch.int32, dev)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    L = _lib.lib()
+    with torch.cuda.device(dev):
+        if n_splits <= 0:
+            n_splits = L.attn_splitkv_auto_splits(B, H, N, d)
+        need = L.attn_splitkv_workspace_bytes(B, H, N, d, int(n_splits))
+        if need == 0:
+            raise ValueError(f"invalid split-KV sizes (n_splits={n_splits})")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the device of q")
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = L.attn_fwd_splitkv(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, B, H, N, d, float(sm_scale),
+            int(bool(causal)), key_lengths.data_ptr() if key_lengths is not None else None,
+            int(n_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            stream)
+    if st != _lib.ATTN_OK:
+        raise _lib.AttnError(st, "attn_fwd_splitkv")
+    return (out, lse) if return_lse else out
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, n_splits: int) -> int:
+    """Workspace bytes fwd_splitkv needs (0 for invalid sizes)."""
+    return int(_lib.lib().attn_splitkv_workspace_bytes(B, H, N, d, n_splits))
+
+
 def _fwd_host(q, k, v, *, causal, sm_scale, key_lengths, return_lse, out, lse_out, path):
     dev = torch.device("cuda", torch.cuda.current_device())
     qd = q.to(dev, non_blocking=True)

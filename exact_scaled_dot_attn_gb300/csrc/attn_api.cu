@@ -4,6 +4,7 @@
 #include "attn_internal.h"
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 
@@ -161,6 +162,102 @@ extern "C" attn_status_t attn_fwd(const void *q, const void *k, const void *v, v
 {
     return attn_fwd_path(q, k, v, o, nullptr, B, H, N, d, sm_scale, causal, key_lengths,
                          ATTN_PATH_AUTO, stream);
+}
+
+namespace {
+
+constexpr int kMaxSplits = 16;
+
+// Bytes of split-KV workspace: fp32 partial outputs [S][B*H*N][d] then logsumexps [S][B*H*N];
+// 0 when the sizes are invalid or the byte count does not fit size_t.
+size_t splitkv_bytes(int B, int H, int N, int d, int S)
+{
+    if (B < 1 || H < 1 || N < 1 || (d != 32 && d != 64 && d != 128) || S < 1 || S > kMaxSplits)
+        return 0;
+    const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+    const unsigned long long per = rows * (static_cast<unsigned long long>(d) + 1) * 4ull;
+    if (rows == 0 || per / rows / 4ull != static_cast<unsigned long long>(d) + 1)
+        return 0;
+    const unsigned long long total = per * static_cast<unsigned long long>(S);
+    if (total / static_cast<unsigned long long>(S) != per || total > static_cast<unsigned long long>(SIZE_MAX))
+        return 0;
+    return static_cast<size_t>(total);
+}
+
+// Ranges per (batch*head, Q tile pair) for the automatic choice: enough units to fill `sms`
+// SMs, at most one range per two K/V tiles of the longest pair, at most kMaxSplits.
+int auto_splits(int B, int H, int N, int sms)
+{
+    const long long pairs = static_cast<long long>(B) * H * ((N + 255) / 256);
+    const int kv_tiles = (N + 127) / 128;
+    int s = 1;
+    while (s < kMaxSplits && pairs * s < sms && (s + 1) * 2 <= kv_tiles)
+        ++s;
+    return s;
+}
+
+} // namespace
+
+extern "C" size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits)
+{
+    return splitkv_bytes(B, H, N, d, n_splits);
+}
+
+extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d)
+{
+    if (B < 1 || H < 1 || N < 1 || (d != 32 && d != 64 && d != 128))
+        return -1;
+    int sms = 0;
+    if (attn::device_sm_count(&sms) != cudaSuccess || sms < 1)
+        sms = 148;
+    return auto_splits(B, H, N, sms);
+}
+
+extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                                          int B, int H, int N, int d, float sm_scale, int causal,
+                                          const int32_t *key_lengths, int n_splits, void *workspace,
+                                          size_t workspace_bytes, attn_stream_t stream)
+{
+    attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
+    if (st != ATTN_OK)
+        return st;
+    if (n_splits <= 0) {
+        n_splits = attn_splitkv_auto_splits(B, H, N, d);
+        if (n_splits < 1)
+            return ATTN_ERR_INVALID_ARG;
+    }
+    if (n_splits > kMaxSplits)
+        return ATTN_ERR_INVALID_ARG;
+    const size_t need = splitkv_bytes(B, H, N, d, n_splits);
+    if (need == 0 || !workspace || workspace_bytes < need)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16))
+        return ATTN_ERR_MISALIGNED;
+    attn::FwdParams p;
+    p.q = static_cast<const __half *>(q);
+    p.k = static_cast<const __half *>(k);
+    p.v = static_cast<const __half *>(v);
+    p.o = static_cast<__half *>(o);
+    p.lse = lse;
+    p.key_lengths = key_lengths;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = d;
+    p.sm_scale = sm_scale;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.causal = causal;
+    p.wait_limit_ns = attn::kDefaultWaitLimitNs;
+    p.inject_missing_arrive = 0;
+    unsigned int *status = nullptr;
+    cudaError_t err = status_word(&status);
+    if (err != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    float *opart = static_cast<float *>(workspace);
+    float *lpart = opart + static_cast<size_t>(n_splits) * B * H * N * d;
+    err = attn::launch_tcgen05_splitkv(p, n_splits, opart, lpart, reinterpret_cast<cudaStream_t>(stream),
+                                       status);
+    return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 extern "C" attn_status_t attn_read_device_status(attn_stream_t stream)

@@ -28,11 +28,20 @@ constexpr unsigned long long kDefaultWaitLimitNs = 4000000000ull;
 // Warp-level mma.sync kernel (every d in {32, 64, 128}, every N).
 cudaError_t launch_warp_mma(const FwdParams &p, cudaStream_t stream);
 
-// TMA + tcgen05/TMEM kernel (d in {64, 128}). `status` is the device status word.
+// TMA + tcgen05/TMEM kernel (d in {32, 64, 128}). `status` is the device status word.
 cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status);
+
+// Split-KV: the tcgen05 kernel over n_splits key ranges per (batch*head, Q tile pair), writing
+// fp32 partial outputs opart [n_splits][B*H*N][d] and logsumexps lpart [n_splits][B*H*N], then
+// the merge kernel writing o (and lse when non-null).
+cudaError_t launch_tcgen05_splitkv(const FwdParams &p, int n_splits, float *opart, float *lpart,
+                                   cudaStream_t stream, unsigned int *status);
 
 // Persistent short-sequence kernel (N <= 256, d in {32, 64}).
 cudaError_t launch_short(const FwdParams &p, cudaStream_t stream, unsigned int *status);
+
+// Multiprocessor count of the current device (cached per device).
+cudaError_t device_sm_count(int *out);
 
 // Status codes the kernels write into the device status word.
 constexpr unsigned int kDevStatusTimeout = 1u;

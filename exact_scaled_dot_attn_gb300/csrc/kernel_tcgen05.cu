@@ -142,8 +142,11 @@ template <int D> struct Cfg {
 struct TcArgs {
     FwdParams p;
     int n_pairs; // ceil(N / 256)
-    int n_units; // n_pairs * B * H
+    int n_units; // n_pairs * B * H * n_splits
     int head_block; // heads per L2 block of the unit order
+    int n_splits;   // key ranges per (batch*head, Q tile pair); 1 outside split-KV
+    float *opart;   // split-KV partial outputs: [split][B*H*N][D] fp32, O / l of the range
+    float *lpart;   // split-KV partial logsumexp: [split][B*H*N] fp32 (-inf: no key in the range)
     unsigned int *status;
 };
 
@@ -151,6 +154,8 @@ struct Unit {
     int bh, b, q0, L;
     int n_kv;       // K/V tiles loaded for the unit (the larger of the two tile counts)
     int n_kv_t[2];  // K/V tiles Q tile t attends to (0 when the tile lies past N)
+    int j0;         // first K/V tile of the unit's key range (split-KV; 0 otherwise)
+    int split;      // index of that range
 };
 
 // Static schedule computed on the host: CTA c processes the units
@@ -169,9 +174,12 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
 {
     const int BH = a.p.B * a.p.H;
     Unit U;
-    const int per_block = a.head_block * a.n_pairs;
+    const int S = a.n_splits;
+    const int per_block = a.head_block * a.n_pairs * S;
     const int blk = u / per_block;
-    const int w = u - blk * per_block;
+    const int ws = u - blk * per_block;
+    const int split = ws % S; // the key ranges of one (head, pair) are adjacent in the order
+    const int w = ws / S;
     const int h0 = blk * a.head_block;
     const int hb = min(a.head_block, BH - h0);
     const int pair = a.n_pairs - 1 - w / hb; // the last query rows carry the most causal work
@@ -189,9 +197,17 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
         kv_end0 = min(L, U.q0 + kBM); // Q tile 0 stops at its own diagonal
         kv_end1 = min(L, U.q0 + 2 * kBM);
     }
-    U.n_kv_t[0] = (kv_end0 + kBN - 1) / kBN;
-    U.n_kv_t[1] = U.q0 + kBM < a.p.N ? (kv_end1 + kBN - 1) / kBN : 0;
-    U.n_kv = max(U.n_kv_t[0], U.n_kv_t[1]);
+    const int full0 = (kv_end0 + kBN - 1) / kBN;
+    const int full1 = U.q0 + kBM < a.p.N ? (kv_end1 + kBN - 1) / kBN : 0;
+    const int n_full = max(full0, full1);
+    // Key range of this split: K/V tiles [j0, j1) of the pair's n_full tiles.
+    const int j0 = split * n_full / S;
+    const int j1 = (split + 1) * n_full / S;
+    U.j0 = j0;
+    U.split = split;
+    U.n_kv_t[0] = max(0, min(j1, full0) - j0);
+    U.n_kv_t[1] = max(0, min(j1, full1) - j0);
+    U.n_kv = j1 - j0;
     return U;
 }
 
@@ -429,7 +445,7 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
     return (a0 + a1) + (b0 + b1);
 }
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tcgen05_kernel(const TcArgs args, const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int bx = 0; bx < D / C::kBoxCols; ++bx)
                             tma_load_3d(sKV + slot * C::kTileBytes + bx * C::kBoxBytes,
                                         kv == 0 ? &tm_k : &tm_v, bar(BB::kKVFull + slot),
-                                        bx * C::kBoxCols, j * kBN, U.bh);
+                                        bx * C::kBoxCols, (U.j0 + j) * kBN, U.bh);
                     }
                     __syncwarp();
                     ++kv_it;
@@ -760,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // softmax step.
         struct Pending {
             bool valid;
-            int bh, row, b;
+            int bh, row, b, split;
             uint32_t last_par; // phase parity of its last PV product in buffer b
             float l, m_ref;
         } pend;
@@ -771,6 +787,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t tO = lane_base + C::tmem_o(t, pe.b);
             const float inv = pe.l > 0.f ? 1.f / pe.l : 0.f;
+            if constexpr (SPLIT) {
+                // The range's O / l in fp32 and its logsumexp, for the merge.
+                const size_t r = static_cast<size_t>(pe.split) * args.p.B * args.p.H * p.N +
+                                 static_cast<size_t>(pe.bh) * p.N + pe.row;
+                float4 *orow = reinterpret_cast<float4 *>(args.opart + r * D);
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c0, ov);
+                    if (pe.row < p.N) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            orow[(c0 + e) >> 2] = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                                              __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(BB::kOEmpty + t * 2 + pe.b));
+                if (pe.row < p.N)
+                    args.lpart[r] = pe.l > 0.f ? (pe.m_ref + log2f(pe.l)) * kLn2 : -INFINITY;
+                return true;
+            }
             __half *orow = p.o + (static_cast<size_t>(pe.bh) * p.N + pe.row) * D;
             constexpr int kChunk = D < 64 ? D : 64; // O columns per TMEM load
 #pragma unroll
@@ -807,7 +845,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Nothing to accumulate: rows with no allowed key get O = 0 and lse = -inf
                 // (rows past N, of a tile that lies beyond the sequence, are not written).
                 const int row = U.q0 + t * kBM + rt;
-                if (row < p.N) {
+                if (SPLIT && row < p.N) {
+                    // no key of this range for the tile: weight 0 in the merge
+                    const size_t r = static_cast<size_t>(U.split) * args.p.B * args.p.H * p.N +
+                                     static_cast<size_t>(U.bh) * p.N + row;
+                    float4 *orow = reinterpret_cast<float4 *>(args.opart + r * D);
+#pragma unroll
+                    for (int c = 0; c < D / 4; ++c)
+                        orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    args.lpart[r] = -INFINITY;
+                } else if (row < p.N) {
                     uint4 z = make_uint4(0, 0, 0, 0);
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(U.bh) * p.N + row) * D);
 #pragma unroll
@@ -831,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++s_it;
                 tc_fence_after();
-                const int kv0 = j * kBN;
+                const int kv0 = (U.j0 + j) * kBN;
                 const bool need_mask = (kv0 + kBN > U.L) || (p.causal && kv0 + kBN - 1 > tile_row0);
                 int lim = U.L - kv0; // keys [kv0, kv0 + lim) are allowed for this row
                 if (p.causal)
@@ -895,6 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             done.bh = U.bh;
             done.row = row;
             done.b = b;
+            done.split = U.split;
             done.last_par = ((pv_par >> b) & 1u) ^ 1u;
             done.l = l;
             done.m_ref = m_ref;
@@ -949,13 +997,15 @@ int head_block_for(int BH, int N, int D)
 
 // Largest-first assignment of the units to the least loaded CTA. The units are taken in
 // the device's unit order (head block by head block, heaviest pair first inside a
-// block), so every CTA works on the same head block at about the same time. The weight
-// of a unit is its count of (Q tile, K/V tile) steps plus a fixed per-unit cost; key
-// lengths are not known on the host and are taken as N.
-void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, int n_pairs, int grid)
+// block, the key ranges of a pair next to each other), so every CTA works on the same head
+// block at about the same time. The weight of a unit is its count of (Q tile, K/V tile)
+// steps plus a fixed per-unit cost; key lengths are not known on the host and are taken as N.
+void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, int n_pairs, int n_splits,
+                    int grid)
 {
-    const int n_units = BH * n_pairs;
-    const int per_block = head_block * n_pairs;
+    const int S = n_splits;
+    const int n_units = BH * n_pairs * S;
+    const int per_block = head_block * n_pairs * S;
     using Slot = std::pair<long long, int>; // (load, cta)
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
     for (int c = 0; c < grid; ++c)
@@ -963,7 +1013,9 @@ void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, in
     std::vector<std::vector<uint16_t>> lists(grid);
     for (int u = 0; u < n_units; ++u) {
         const int blk = u / per_block;
-        const int w = u - blk * per_block;
+        const int ws = u - blk * per_block;
+        const int split = ws % S;
+        const int w = ws / S;
         const int hb = std::min(head_block, BH - blk * head_block);
         const int pair = n_pairs - 1 - w / hb;
         const int q0 = pair * 2 * kBM;
@@ -972,13 +1024,17 @@ void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, in
             e0 = std::min(N, q0 + kBM);
             e1 = std::min(N, q0 + 2 * kBM);
         }
-        const int n0 = (e0 + kBN - 1) / kBN;
-        const int n1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
+        const int f0 = (e0 + kBN - 1) / kBN;
+        const int f1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
+        const int nf = std::max(f0, f1);
+        const int j0 = split * nf / S, j1 = (split + 1) * nf / S;
+        const int n0 = std::max(0, std::min(j1, f0) - j0);
+        const int n1 = std::max(0, std::min(j1, f1) - j0);
         const long long weight = n0 + n1 + 2;
-        Slot s = heap.top();
+        Slot sl = heap.top();
         heap.pop();
-        lists[s.second].push_back(static_cast<uint16_t>(u));
-        heap.push({s.first + weight, s.second});
+        lists[sl.second].push_back(static_cast<uint16_t>(u));
+        heap.push({sl.first + weight, sl.second});
     }
     t.use = 1;
     int k = 0;
@@ -990,30 +1046,33 @@ void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, in
     t.off[grid] = static_cast<uint16_t>(k);
 }
 
-// Schedules are cached per shape (they depend on B*H, N, d, causal and the SM count only).
+// Schedules are cached per shape (they depend on B*H, N, d, causal, the split count and the
+// SM count only).
 std::mutex g_sched_mutex;
-std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
+std::map<std::tuple<int, int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
 
 std::shared_ptr<SchedTable> schedule_for(int BH, int N, int D, int causal, int head_block, int n_pairs,
-                                         int grid)
+                                         int n_splits, int grid)
 {
-    auto key = std::make_tuple(BH, N, D, causal, grid);
+    auto key = std::make_tuple(BH, N, D, causal, n_splits, grid);
     std::lock_guard<std::mutex> lock(g_sched_mutex);
     auto it = g_sched_cache.find(key);
     if (it != g_sched_cache.end())
         return it->second;
     auto t = std::make_shared<SchedTable>();
     memset(t.get(), 0, sizeof(SchedTable));
-    const long long n_units = static_cast<long long>(BH) * n_pairs;
+    const long long n_units = static_cast<long long>(BH) * n_pairs * n_splits;
     if (grid <= kMaxCtas && n_units <= kMaxSchedUnits)
-        build_schedule(*t, BH, N, causal, head_block, n_pairs, grid);
+        build_schedule(*t, BH, N, causal, head_block, n_pairs, n_splits, grid);
     if (g_sched_cache.size() >= 64)
         g_sched_cache.clear();
     g_sched_cache[key] = t;
     return t;
 }
 
-template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, unsigned int *status)
+template <int D, bool SPLIT>
+cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpart, cudaStream_t stream,
+                     unsigned int *status)
 {
     using C = Cfg<D>;
     const int BH = p.B * p.H;
@@ -1024,31 +1083,94 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
     TcArgs a;
     a.p = p;
     a.n_pairs = (p.N + 2 * kBM - 1) / (2 * kBM);
-    const long long units = static_cast<long long>(a.n_pairs) * BH;
+    const long long units = static_cast<long long>(a.n_pairs) * BH * n_splits;
     if (units > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     a.n_units = static_cast<int>(units);
     a.head_block = head_block_for(BH, p.N, D);
+    a.n_splits = n_splits;
+    a.opart = opart;
+    a.lpart = lpart;
     a.status = status;
     int sms = 0;
     cudaError_t err = device_sm_count(&sms);
     if (err != cudaSuccess)
         return err;
-    err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::kSmemBytes);
+    auto kernel = attn_fwd_tcgen05_kernel<D, SPLIT>;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess)
         return err;
     // The register split inside the kernel must fit the pool the CTA is launched with.
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, attn_fwd_tcgen05_kernel<D>);
+    err = cudaFuncGetAttributes(&fa, kernel);
     if (err != cudaSuccess)
         return err;
     if (static_cast<long long>(fa.numRegs) * kThreads < RegSplit<D>::kPoolNeeded)
         return cudaErrorInvalidConfiguration;
     const int grid = a.n_units < sms ? a.n_units : sms;
     std::shared_ptr<SchedTable> sched =
-        schedule_for(BH, p.N, D, p.causal, a.head_block, a.n_pairs, grid);
-    attn_fwd_tcgen05_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
+        schedule_for(BH, p.N, D, p.causal, a.head_block, a.n_pairs, n_splits, grid);
+    kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
+    return cudaGetLastError();
+}
+
+// Combination of the key ranges of split-KV for one row per warp, by the merge of two partial
+// softmaxes of "Online Softmax Formulation" applied to S ranges at once: with lse_s the
+// logsumexp of range s and O_s its normalised output, lse = log sum_s exp(lse_s) and
+// O = sum_s exp(lse_s - lse) O_s. Ranges without an allowed key (lse_s = -inf) weigh 0; a
+// row with none at all gets O = 0 and lse = -inf.
+template <int D>
+__global__ void __launch_bounds__(256)
+    attn_splitkv_merge_kernel(const float *__restrict__ opart, const float *__restrict__ lpart,
+                              __half *__restrict__ o, float *__restrict__ lse, long long rows, int S)
+{
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows)
+        return;
+    const float ls = lane < S ? lpart[static_cast<long long>(lane) * rows + row] : -INFINITY;
+    float m = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float ws = (m == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - m);
+    float wsum = ws;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    constexpr int kPer = D / 32; // output columns of this lane: [lane * kPer, lane * kPer + kPer)
+    float acc[kPer];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c)
+        acc[c] = 0.f;
+    for (int s = 0; s < S; ++s) {
+        const float w = __shfl_sync(0xffffffffu, ws, s);
+        if (w == 0.f)
+            continue;
+        const float *src = opart + (static_cast<long long>(s) * rows + row) * D + lane * kPer;
+#pragma unroll
+        for (int c = 0; c < kPer; ++c)
+            acc[c] += w * src[c];
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __half *dst = o + row * D + lane * kPer;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c)
+        dst[c] = __float2half_rn(acc[c] * inv);
+    if (lse && lane == 0)
+        lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_merge(const FwdParams &p, int n_splits, const float *opart, const float *lpart,
+                         cudaStream_t stream)
+{
+    const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    attn_splitkv_merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        opart, lpart, p.o, p.lse, rows, n_splits);
     return cudaGetLastError();
 }
 
@@ -1057,10 +1179,29 @@ template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream, u
 cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
     switch (p.d) {
-    case 32: return launch_d<32>(p, stream, status);
-    case 64: return launch_d<64>(p, stream, status);
-    case 128: return launch_d<128>(p, stream, status);
+    case 32: return launch_d<32, false>(p, 1, nullptr, nullptr, stream, status);
+    case 64: return launch_d<64, false>(p, 1, nullptr, nullptr, stream, status);
+    case 128: return launch_d<128, false>(p, 1, nullptr, nullptr, stream, status);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_tcgen05_splitkv(const FwdParams &p, int n_splits, float *opart, float *lpart,
+                                   cudaStream_t stream, unsigned int *status)
+{
+    cudaError_t err;
+    switch (p.d) {
+    case 32: err = launch_d<32, true>(p, n_splits, opart, lpart, stream, status); break;
+    case 64: err = launch_d<64, true>(p, n_splits, opart, lpart, stream, status); break;
+    case 128: err = launch_d<128, true>(p, n_splits, opart, lpart, stream, status); break;
+    default: return cudaErrorInvalidValue;
+    }
+    if (err != cudaSuccess)
+        return err;
+    switch (p.d) {
+    case 32: return launch_merge<32>(p, n_splits, opart, lpart, stream);
+    case 64: return launch_merge<64>(p, n_splits, opart, lpart, stream);
+    default: return launch_merge<128>(p, n_splits, opart, lpart, stream);
     }
 }
 

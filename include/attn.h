@@ -43,6 +43,7 @@
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -116,6 +117,38 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
                              int B, int H, int N, int d, float sm_scale, int causal,
                              const int32_t *key_lengths, int path, const attn_debug_opts_t *opts,
                              attn_stream_t stream);
+
+/*
+ * Split-KV forward: the same result as attn_fwd_lse (lse may be NULL), computed with the keys
+ * of every (batch*head, pair of 128-row query tiles) divided into n_splits contiguous ranges of
+ * 128-key tiles that run as separate work units (more parallel work when B*H*ceil(N/256) is
+ * below the SM count, e.g. one long sequence), followed by a merge of the ranges. The merge is
+ * the combination of two partial softmaxes of "Self-Attention Kernel & Inference Engine from
+ * Scratch" ("Online Softmax Formulation") applied to n_splits ranges at once: with lse_s the
+ * logsumexp of range s and O_s its normalised output, lse = log sum_s exp(lse_s) and
+ * O = sum_s exp(lse_s - lse) O_s.
+ *   n_splits         1..16, or <= 0 for attn_splitkv_auto_splits(B, H, N, d)
+ *   workspace        device memory of at least attn_splitkv_workspace_bytes(B, H, N, d, n_splits)
+ *                    bytes, 16-byte aligned, owned by the caller; its contents on entry do not
+ *                    matter and on return are undefined. Launches that share a workspace must
+ *                    not overlap on the device.
+ * The other arguments, layouts and errors are those of attn_fwd_lse; a missing or too small
+ * workspace or n_splits > 16 gives ATTN_ERR_INVALID_ARG, a misaligned one ATTN_ERR_MISALIGNED.
+ * Runs the tcgen05 kernel (every d in {32, 64, 128}, every N) and one merge kernel.
+ */
+attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int B, int H, int N, int d, float sm_scale, int causal,
+                               const int32_t *key_lengths, int n_splits, void *workspace,
+                               size_t workspace_bytes, attn_stream_t stream);
+
+/* Workspace bytes attn_fwd_splitkv needs: n_splits * B*H*N * (d + 1) * 4 (fp32 partial
+ * outputs and logsumexps of every range). 0 for invalid sizes or n_splits outside 1..16. */
+size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
+
+/* The split count attn_fwd_splitkv uses for n_splits <= 0: the smallest count that gives at
+ * least one (Q tile pair, key range) unit per SM of the current device, at most one range per
+ * two 128-key tiles of the sequence and at most 16. -1 for invalid sizes. */
+int attn_splitkv_auto_splits(int B, int H, int N, int d);
 
 /* The kernel ATTN_PATH_AUTO selects for sequence length N and head dimension d
  * (an attn_path_t value), or -1 when d is unsupported. No CUDA call is made. */

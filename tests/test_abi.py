@@ -96,3 +96,28 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _lib.lib()
+
+
+def test_splitkv_workspace_bytes(lib):
+    # n_splits * B*H*N * (d + 1) * 4
+    assert lib.attn_splitkv_workspace_bytes(2, 3, 100, 64, 4) == 4 * 2 * 3 * 100 * 65 * 4
+    assert lib.attn_splitkv_workspace_bytes(1, 1, 1, 128, 1) == 129 * 4
+    for bad in [(0, 1, 8, 64, 1), (1, 1, 8, 48, 1), (1, 1, 8, 64, 0), (1, 1, 8, 64, 17)]:
+        assert lib.attn_splitkv_workspace_bytes(*bad) == 0
+
+
+def test_splitkv_validation(lib):
+    def sk(n_splits=2, ws=A, ws_bytes=1 << 30, **kw):
+        args = dict(q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=256, d=64, scale=0.125, causal=0,
+                    kl=None)
+        args.update(kw)
+        return lib.attn_fwd_splitkv(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                    args["B"], args["H"], args["N"], args["d"], args["scale"],
+                                    args["causal"], args["kl"], n_splits, ws, ws_bytes, None)
+    need = lib.attn_splitkv_workspace_bytes(1, 1, 256, 64, 2)
+    assert sk(ws=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert sk(ws_bytes=need - 1) == _lib.ATTN_ERR_INVALID_ARG
+    assert sk(n_splits=17) == _lib.ATTN_ERR_INVALID_ARG
+    assert sk(ws=A + 4, ws_bytes=need) == _lib.ATTN_ERR_MISALIGNED
+    assert sk(d=48) == _lib.ATTN_ERR_UNSUPPORTED
+    assert sk(q=None) == _lib.ATTN_ERR_INVALID_ARG
