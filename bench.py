@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05", "short"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short-n", action="store_true")
+    ap.add_argument("--no-split-kv", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
 
@@ -366,6 +367,8 @@ def main():
 
     if not args.no_short_n:
         line["short_n"] = short_n(torch, api, peaks, peak_src)
+    if not args.no_split_kv:
+        line["split_kv"] = split_kv(torch, api, peaks, peak_src)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # Bounded sample of the same workload: the first heads (flat batch*head order), all
@@ -448,6 +451,40 @@ def short_n(torch, api, peaks, peak_src):
             "flushed_single_launch": {"ms": flushed_ms,
                                       "value": nbytes / (flushed_ms * 1e-3) / 1e9, "unit": "GB/s",
                                       "l2": "flushed (512 MiB write) before the launch"}}
+
+
+def split_kv(torch, api, peaks, peak_src):
+    """One long causal head (B=1, H=1, N=32768, d=128): fewer query tile pairs than SMs. The
+    tiled kernel alone against split-KV with the automatic split count, TFLOP/s of the contract
+    count; L2 flushed before every timed launch (the inputs are smaller than L2)."""
+    w = synth.WORKLOADS["one_head"]
+    q, k, v, _ = synth.draw_workload(w)
+    qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    od = torch.empty_like(qd)
+    flops = synth.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    n_splits = int(api._lib.lib().attn_splitkv_auto_splits(w.B, w.H, w.N, w.d, int(w.causal)))
+    ws = torch.empty(api.splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits), dtype=torch.uint8,
+                     device="cuda")
+    flush = l2_flush_buffer(torch)
+
+    def unsplit():
+        api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od, path="tcgen05")
+
+    def split():
+        api.fwd_splitkv(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od,
+                        n_splits=n_splits, workspace=ws)
+
+    res = {}
+    for name, fn in (("unsplit", unsplit), ("split", split)):
+        time_launches(torch, fn, 3, flush)
+        res[name] = statistics.median(time_launches(torch, fn, 20, flush))
+    tf = {k2: flops / (ms * 1e-3) / 1e12 for k2, ms in res.items()}
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {"workload": w.describe(), "value": tf["split"], "unit": "TFLOP/s", "n_splits": n_splits,
+            "launch_ms": res["split"], "unsplit_value": tf["unsplit"], "unsplit_launch_ms": res["unsplit"],
+            "roofline": {"bound": "tensor", "achieved": tf["split"], "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf["split"] / peak, "peak_source": f"{peak_src} bf16 dense burst"},
+            "l2": "flushed (512 MiB write) before every timed launch; the split launch includes the merge kernel"}
 
 
 if __name__ == "__main__":

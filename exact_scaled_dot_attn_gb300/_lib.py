@@ -42,7 +42,7 @@ SIGNATURES = {
     "attn_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp,
                               ctypes.c_size_t, _vp]),
     "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
-    "attn_splitkv_auto_splits": (_i, [_i, _i, _i, _i]),
+    "attn_splitkv_auto_splits": (_i, [_i, _i, _i, _i, _i]),
 }
 
 _lib = None

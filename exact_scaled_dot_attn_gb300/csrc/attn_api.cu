@@ -184,16 +184,21 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S)
     return static_cast<size_t>(total);
 }
 
-// Ranges per (batch*head, Q tile pair) for the automatic choice: enough units to fill `sms`
-// SMs, at most one range per two K/V tiles of the longest pair, at most kMaxSplits.
-int auto_splits(int B, int H, int N, int sms)
+// Ranges per (batch*head, Q tile pair) for the automatic choice: enough (pair, range) units
+// that the largest one is no longer than an SM's average share. Without a causal mask every
+// pair has the same work and one unit per SM suffices; with it the largest pair has about
+// twice the average. At most one range per two K/V tiles, at most kMaxSplits.
+int auto_splits(int B, int H, int N, int causal, int sms)
 {
     const long long pairs = static_cast<long long>(B) * H * ((N + 255) / 256);
+    const long long want = (static_cast<long long>(sms) * (causal ? 2 : 1) + pairs - 1) / pairs;
     const int kv_tiles = (N + 127) / 128;
-    int s = 1;
-    while (s < kMaxSplits && pairs * s < sms && (s + 1) * 2 <= kv_tiles)
-        ++s;
-    return s;
+    long long s = want < 1 ? 1 : want;
+    if (s > kv_tiles / 2)
+        s = kv_tiles / 2;
+    if (s > kMaxSplits)
+        s = kMaxSplits;
+    return s < 1 ? 1 : static_cast<int>(s);
 }
 
 } // namespace
@@ -203,14 +208,14 @@ extern "C" size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n
     return splitkv_bytes(B, H, N, d, n_splits);
 }
 
-extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d)
+extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal)
 {
-    if (B < 1 || H < 1 || N < 1 || (d != 32 && d != 64 && d != 128))
+    if (B < 1 || H < 1 || N < 1 || (d != 32 && d != 64 && d != 128) || (causal != 0 && causal != 1))
         return -1;
     int sms = 0;
     if (attn::device_sm_count(&sms) != cudaSuccess || sms < 1)
         sms = 148;
-    return auto_splits(B, H, N, sms);
+    return auto_splits(B, H, N, causal, sms);
 }
 
 extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -222,7 +227,7 @@ extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const vo
     if (st != ATTN_OK)
         return st;
     if (n_splits <= 0) {
-        n_splits = attn_splitkv_auto_splits(B, H, N, d);
+        n_splits = attn_splitkv_auto_splits(B, H, N, d, causal);
         if (n_splits < 1)
             return ATTN_ERR_INVALID_ARG;
     }

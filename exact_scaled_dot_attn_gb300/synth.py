@@ -59,6 +59,9 @@ WORKLOADS = {
     "prefill": Workload("prefill", 4, 32, 4096, 128, True, seed=3),
     "long": Workload("long", 1, 32, 32768, 128, True, seed=4),
     "stress": Workload("stress", 2, 16, 8192, 64, False, seed=5, sigma_qk=3.0, check_lse=True),
+    # one long causal sequence of a single head: fewer query tile pairs than SMs (the case the
+    # split-KV path is for)
+    "one_head": Workload("one_head", 1, 1, 32768, 128, True, seed=6),
 }
 
 

@@ -127,7 +127,7 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
  * Scratch" ("Online Softmax Formulation") applied to n_splits ranges at once: with lse_s the
  * logsumexp of range s and O_s its normalised output, lse = log sum_s exp(lse_s) and
  * O = sum_s exp(lse_s - lse) O_s.
- *   n_splits         1..16, or <= 0 for attn_splitkv_auto_splits(B, H, N, d)
+ *   n_splits         1..16, or <= 0 for attn_splitkv_auto_splits(B, H, N, d, causal)
  *   workspace        device memory of at least attn_splitkv_workspace_bytes(B, H, N, d, n_splits)
  *                    bytes, 16-byte aligned, owned by the caller; its contents on entry do not
  *                    matter and on return are undefined. Launches that share a workspace must
@@ -145,10 +145,11 @@ attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void
  * outputs and logsumexps of every range). 0 for invalid sizes or n_splits outside 1..16. */
 size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 
-/* The split count attn_fwd_splitkv uses for n_splits <= 0: the smallest count that gives at
- * least one (Q tile pair, key range) unit per SM of the current device, at most one range per
- * two 128-key tiles of the sequence and at most 16. -1 for invalid sizes. */
-int attn_splitkv_auto_splits(int B, int H, int N, int d);
+/* The split count attn_fwd_splitkv uses for n_splits <= 0: enough (Q tile pair, key range)
+ * units that the largest is no longer than an SM's average share on the current device (one
+ * unit per SM without a causal mask, two with it, where the last pair has twice the average
+ * work), at most one range per two 128-key tiles and at most 16. -1 for invalid sizes. */
+int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
 /* The kernel ATTN_PATH_AUTO selects for sequence length N and head dimension d
  * (an attn_path_t value), or -1 when d is unsupported. No CUDA call is made. */
