@@ -13,6 +13,7 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_SCRATCH_LIMIT = 6
 
 PATH_AUTO = 0
 PATH_WARP_MMA = 1
@@ -43,6 +44,8 @@ SIGNATURES = {
                               ctypes.c_size_t, _vp]),
     "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
     "attn_splitkv_auto_splits": (_i, [_i, _i, _i, _i, _i]),
+    "attn_fwd_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
 }
 
 _lib = None

@@ -77,6 +77,7 @@ extern "C" const char *attn_status_str(attn_status_t status)
     case ATTN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "bounded on-chip wait ran out";
+    case ATTN_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
     }
 }
@@ -263,6 +264,80 @@ extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const vo
     err = attn::launch_tcgen05_splitkv(p, n_splits, opart, lpart, reinterpret_cast<cudaStream_t>(stream),
                                        status);
     return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- split-KV without allocation
+//
+// Some callers cannot allocate device memory on the path that calls the attention: a serving
+// process whose device memory is already handed out to its own pool or caching allocator (a
+// cudaMalloc there fails, or takes memory the pool counted on), a plug-in running inside
+// another runtime that gives it no allocator, or a latency-bound request loop where the
+// implicit synchronisation of cudaMalloc/cudaFree is not acceptable. For them the split-KV
+// forward can run on a fixed scratch array that is part of this library's device image: the
+// caller passes only inputs and outputs.
+namespace {
+
+// The scratch array (fp32 partial outputs, then partial logsumexps). Every GPU on which the
+// library's device code is loaded holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once per device with
+// that device current.
+cudaError_t noalloc_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess)
+            return err;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+} // namespace
+
+extern "C" size_t attn_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
+                                                  float *lse, int B, int H, int N, int d, float sm_scale,
+                                                  int causal, const int32_t *key_lengths, int n_splits,
+                                                  attn_stream_t stream)
+{
+    attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
+    if (st != ATTN_OK)
+        return st;
+    if (n_splits <= 0) {
+        n_splits = attn_splitkv_auto_splits(B, H, N, d, causal);
+        if (n_splits < 1)
+            return ATTN_ERR_INVALID_ARG;
+    }
+    if (n_splits > kMaxSplits)
+        return ATTN_ERR_INVALID_ARG;
+    const size_t need = splitkv_bytes(B, H, N, d, n_splits);
+    if (need == 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (need > kNoAllocScratchBytes)
+        return ATTN_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    // Nothing in the array needs clearing: the split kernel writes every partial output and
+    // logsumexp the merge reads, in this call.
+    return attn_fwd_splitkv(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths, n_splits, scratch,
+                            kNoAllocScratchBytes, stream);
 }
 
 extern "C" attn_status_t attn_read_device_status(attn_stream_t stream)

@@ -59,7 +59,9 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 2, /* head dimension other than 32, 64 or 128; unknown path */
     ATTN_ERR_MISALIGNED = 3,  /* a tensor pointer that is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
-    ATTN_ERR_TIMEOUT = 5      /* a bounded on-chip wait ran out (see attn_read_device_status) */
+    ATTN_ERR_TIMEOUT = 5,     /* a bounded on-chip wait ran out (see attn_read_device_status) */
+    ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_fwd_splitkv_noalloc: the problem needs more scratch than
+                                  attn_noalloc_scratch_bytes() */
 } attn_status_t;
 
 /* Which kernel runs the forward. AUTO runs the short-sequence kernel for d = 32 with
@@ -150,6 +152,33 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
  * unit per SM without a causal mask, two with it, where the last pair has twice the average
  * work), at most one range per two 128-key tiles and at most 16. -1 for invalid sizes. */
 int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal);
+
+/*
+ * Split-KV forward that allocates nothing (the pages have no counterpart: this is a service of
+ * the library). For callers that cannot allocate device memory where they call the attention:
+ * a serving process whose device memory already belongs to its own pool or caching allocator,
+ * a plug-in hosted by a runtime that gives it no allocator, or a latency-bound loop that cannot
+ * pay the synchronisation of cudaMalloc/cudaFree. It is attn_fwd_splitkv with its workspace
+ * in a fixed array of attn_noalloc_scratch_bytes() bytes (64 MiB) that is part of the
+ * library's device code: every GPU on which the library is loaded holds that array until the
+ * process exits. The caller passes inputs and outputs only; nothing is allocated, by this
+ * library or by any library it calls.
+ *   - A problem whose split-KV workspace (attn_splitkv_workspace_bytes) exceeds the array
+ *     returns ATTN_ERR_SCRATCH_LIMIT before any launch; use fewer splits or attn_fwd_splitkv.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents (no
+ *     part of it needs clearing: each call writes all it reads). Calls whose executions overlap
+ *     on the same GPU (different streams, concurrent host threads) race on it and must be
+ *     ordered by the caller.
+ * Arguments and the other errors are those of attn_fwd_splitkv without the workspace.
+ */
+attn_status_t attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                       int B, int H, int N, int d, float sm_scale, int causal,
+                                       const int32_t *key_lengths, int n_splits, attn_stream_t stream);
+
+/* Bytes of the fixed scratch array of attn_fwd_splitkv_noalloc (64 MiB). */
+size_t attn_noalloc_scratch_bytes(void);
 
 /* The kernel ATTN_PATH_AUTO selects for sequence length N and head dimension d
  * (an attn_path_t value), or -1 when d is unsupported. No CUDA call is made. */

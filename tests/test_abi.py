@@ -43,7 +43,7 @@ def test_every_declared_symbol_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, 6):
+    for code in range(0, 7):
         s = _lib.status_str(code)
         assert s and s != "unknown status"
     assert _lib.status_str(99) == "unknown status"
@@ -121,3 +121,16 @@ def test_splitkv_validation(lib):
     assert sk(ws=A + 4, ws_bytes=need) == _lib.ATTN_ERR_MISALIGNED
     assert sk(d=48) == _lib.ATTN_ERR_UNSUPPORTED
     assert sk(q=None) == _lib.ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_limit(lib):
+    """The no-allocation split-KV entry point states its fixed scratch size and rejects a
+    problem that needs more, before any launch."""
+    cap = lib.attn_noalloc_scratch_bytes()
+    assert cap == 64 << 20
+    B, H, N, d, S = 1, 8, 32768, 128, 4
+    assert lib.attn_splitkv_workspace_bytes(B, H, N, d, S) > cap
+    st = lib.attn_fwd_splitkv_noalloc(A, A, A, A, None, B, H, N, d, 0.088, 1, None, S, None)
+    assert st == _lib.ATTN_ERR_SCRATCH_LIMIT
+    assert lib.attn_fwd_splitkv_noalloc(A, A, A, A, None, 1, 1, 256, 64, 0.125, 0, None, 17,
+                                        None) == _lib.ATTN_ERR_INVALID_ARG
