@@ -50,6 +50,13 @@ class Oracle:
             ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
+        lib.oracle_attn_ex.restype = ctypes.c_int
+        lib.oracle_attn_ex.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ]
         self._lib = lib
 
     def half_to_double(self, bits: int) -> float:
@@ -60,7 +67,10 @@ class Oracle:
              rows=None, threads: int | None = None):
         """Oracle forward.
 
-        q, k, v: numpy float16 arrays of shape [B, H, N, d].
+        q: numpy float16 array [B, H, N, d] (N query rows per head); k, v: [B, Hkv, Nk, d]
+        with H a multiple of Hkv (query head h reads key/value head h // (H // Hkv)).
+        Self-attention is k, v of q's shape. With causal and Nk != N, query i sees
+        keys j <= i + Nk - N.
         key_lengths: int array [B] or None. rows: ascending flat row ids
         ((b*H + h)*N + i) or None for every row.
         Returns (o, lse) as float64: o is [B,H,N,d] (or [len(rows), d]), lse is
@@ -69,9 +79,12 @@ class Oracle:
         q = np.ascontiguousarray(q, dtype=np.float16)
         k = np.ascontiguousarray(k, dtype=np.float16)
         v = np.ascontiguousarray(v, dtype=np.float16)
-        if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
-            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape:
+            raise ValueError("q must be [B,H,N,d] and k, v one [B,Hkv,Nk,d] shape")
         B, H, N, d = q.shape
+        Hkv, Nk = k.shape[1], k.shape[2]
+        if k.shape[0] != B or k.shape[3] != d or Hkv < 1 or H % Hkv != 0:
+            raise ValueError("k, v must be [B,Hkv,Nk,d] with H a multiple of Hkv")
         kl = None
         if key_lengths is not None:
             kl = np.ascontiguousarray(key_lengths, dtype=np.int32)
@@ -87,13 +100,13 @@ class Oracle:
             n_rows = rows_arr.size
             o = np.empty((n_rows, d), np.float64)
             lse = np.empty((n_rows,), np.float64)
-        rc = self._lib.oracle_attn(
-            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, N, d, float(sm_scale),
+        rc = self._lib.oracle_attn_ex(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Hkv, N, Nk, d, float(sm_scale),
             int(bool(causal)), None if kl is None else kl.ctypes.data,
             None if rows_arr is None else rows_arr.ctypes.data, n_rows,
             o.ctypes.data, lse.ctypes.data, int(threads or default_threads()))
         if rc != 0:
-            raise RuntimeError(f"oracle_attn failed with code {rc}")
+            raise RuntimeError(f"oracle_attn_ex failed with code {rc}")
         return o, lse
 
 

@@ -6,11 +6,13 @@
  * and its Python binding) never calls it, and this file includes nothing from
  * the product path.
  *
- * What it computes, for every batch b, head h and query row i (self-attention,
- * N queries and N keys per head, inputs fp16 in [B,H,N,d] layout, d innermost):
+ * What it computes, for every batch b, query head h and query row i (inputs fp16,
+ * d innermost; Q and O [B,H,Nq,d], K and V [B,Hkv,Nk,d]; query head h reads key/value
+ * head h / (H / Hkv), grouped-query attention, Hkv = H being multi-head attention;
+ * self-attention is Nq = Nk = N):
  *
- *   allowed set   A_i = { j : j < L_b  and  (not causal or j <= i) }
- *                 L_b = clamp(key_lengths[b], 0, N), or N when no lengths are given
+ *   allowed set   A_i = { j : j < L_b  and  (not causal or j <= i + Nk - Nq) }
+ *                 L_b = clamp(key_lengths[b], 0, Nk), or Nk when no lengths are given
  *   scores        s_ij = sm_scale * sum_c q_ic k_jc                      (j in A_i)
  *   row max       m_i  = max_{j in A_i} s_ij
  *   normaliser    l_i  = sum_{j in A_i} exp(s_ij - m_i)
@@ -33,7 +35,12 @@
  *     keys are excluded from each row's softmax.
  *   - causal: query i attends to keys j <= i (square, top-left aligned), the
  *     plain reading of the causal block skip in "Engineering Decisions &
- *     Trade-offs" of the portfolio page.
+ *     Trade-offs" of the portfolio page. With Nq != Nk (cross-attention, one of
+ *     the README's "natural extensions") the diagonal is aligned at the last
+ *     rows: query i sees keys j <= i + Nk - Nq, so the last query sees every
+ *     key. The pages fix no alignment; this is the reading taken.
+ *   - grouped-query attention (the other "natural extension"): query heads are
+ *     split into Hkv consecutive groups of H / Hkv heads, each sharing one K, V.
  *   - logsumexp is not on the pages; it is the natural log of the softmax
  *     normaliser over the scaled, allowed scores.
  *
@@ -75,25 +82,25 @@ static void build_half_table(void)
         g_half_table[h] = oracle_half_to_double((uint16_t)h);
 }
 
-/* Key j is in query i's allowed set. */
-static int allowed(int64_t i, int64_t j, int64_t L, int causal)
+/* Key j is in query i's allowed set; off = Nk - Nq places the causal diagonal. */
+static int allowed(int64_t i, int64_t j, int64_t L, int causal, int64_t off)
 {
     if (j >= L)
         return 0; /* key padding: keys at or past the valid length are excluded */
-    if (causal && j > i)
-        return 0; /* causal: query i sees keys j <= i only */
+    if (causal && j > i + off)
+        return 0; /* causal: query i sees keys j <= i + Nk - Nq only */
     return 1;
 }
 
-/* One query row. q: [d]; K, V: [N, d] decoded; s: scratch [N]; o: [d] out. */
+/* One query row. q: [d]; K, V: [N, d] decoded (N keys); s: scratch [N]; o: [d] out. */
 static void attention_row(const double *q, const double *K, const double *V, int64_t N, int64_t d,
-                          double sm_scale, int64_t i, int64_t L, int causal, double *s, double *o,
-                          double *lse)
+                          double sm_scale, int64_t i, int64_t L, int causal, int64_t off,
+                          double *s, double *o, double *lse)
 {
     int any = 0;
     double m = -INFINITY;
     for (int64_t j = 0; j < N; ++j) {
-        if (!allowed(i, j, L, causal))
+        if (!allowed(i, j, L, causal, off))
             continue;
         double dot = 0.0;
         for (int64_t c = 0; c < d; ++c)
@@ -111,10 +118,10 @@ static void attention_row(const double *q, const double *K, const double *V, int
     }
     double l = 0.0;
     for (int64_t j = 0; j < N; ++j)
-        if (allowed(i, j, L, causal))
+        if (allowed(i, j, L, causal, off))
             l += exp(s[j] - m);
     for (int64_t j = 0; j < N; ++j) {
-        if (!allowed(i, j, L, causal))
+        if (!allowed(i, j, L, causal, off))
             continue;
         double p = exp(s[j] - m) / l;
         for (int64_t c = 0; c < d; ++c)
@@ -125,7 +132,8 @@ static void attention_row(const double *q, const double *K, const double *V, int
 
 typedef struct {
     const uint16_t *q, *k, *v;
-    int64_t B, H, N, d;
+    int64_t B, H, N, d; /* N: query rows per head */
+    int64_t Hkv, Nk;    /* key/value heads per batch, keys per head */
     double sm_scale;
     int causal;
     const int32_t *key_lengths;
@@ -145,10 +153,11 @@ static int64_t row_id(const job_t *J, int64_t t) { return J->rows ? J->rows[t] :
 static void *worker(void *arg)
 {
     job_t *J = (job_t *)arg;
-    const int64_t N = J->N, d = J->d;
-    double *K = (double *)malloc((size_t)(N * d) * sizeof(double));
-    double *V = (double *)malloc((size_t)(N * d) * sizeof(double));
-    double *s = (double *)malloc((size_t)N * sizeof(double));
+    const int64_t N = J->N, d = J->d, Nk = J->Nk, G = J->H / J->Hkv;
+    const size_t kv_elems = (size_t)(Nk > 0 ? Nk * d : 1);
+    double *K = (double *)malloc(kv_elems * sizeof(double));
+    double *V = (double *)malloc(kv_elems * sizeof(double));
+    double *s = (double *)malloc((size_t)(Nk > 0 ? Nk : 1) * sizeof(double));
     double *q = (double *)malloc((size_t)d * sizeof(double));
     int64_t decoded_head = -1;
     if (!K || !V || !s || !q) {
@@ -167,26 +176,28 @@ static void *worker(void *arg)
         int64_t t0 = J->item_begin[it], t1 = J->item_begin[it + 1];
         for (int64_t t = t0; t < t1; ++t) {
             int64_t r = row_id(J, t);
-            int64_t bh = r / N, i = r % N, b = bh / J->H;
-            if (bh != decoded_head) {
-                const uint16_t *kh = J->k + bh * N * d, *vh = J->v + bh * N * d;
-                for (int64_t e = 0; e < N * d; ++e) {
+            int64_t bh = r / N, i = r % N, b = bh / J->H, h = bh % J->H;
+            int64_t kvh = b * J->Hkv + h / G; /* the key/value head query head h reads */
+            if (kvh != decoded_head) {
+                const uint16_t *kh = J->k + kvh * Nk * d, *vh = J->v + kvh * Nk * d;
+                for (int64_t e = 0; e < Nk * d; ++e) {
                     K[e] = g_half_table[kh[e]];
                     V[e] = g_half_table[vh[e]];
                 }
-                decoded_head = bh;
+                decoded_head = kvh;
             }
             const uint16_t *qr = J->q + r * d;
             for (int64_t c = 0; c < d; ++c)
                 q[c] = g_half_table[qr[c]];
-            int64_t L = N;
+            int64_t L = Nk;
             if (J->key_lengths) {
                 L = J->key_lengths[b];
                 if (L < 0) L = 0;
-                if (L > N) L = N;
+                if (L > Nk) L = Nk;
             }
             double lse;
-            attention_row(q, K, V, N, d, J->sm_scale, i, L, J->causal, s, J->o + t * d, &lse);
+            attention_row(q, K, V, Nk, d, J->sm_scale, i, L, J->causal, Nk - N, s, J->o + t * d,
+                          &lse);
             if (J->lse)
                 J->lse[t] = lse;
         }
@@ -196,18 +207,21 @@ static void *worker(void *arg)
 }
 
 /*
- * Computes O (and lse) for the listed query rows, or for all B*H*N rows when
- * rows == NULL. q, k, v: fp16 bit patterns [B,H,N,d]. key_lengths: [B] or NULL.
- * rows: flat row ids (b*H + h)*N + i in ascending order, n_rows of them.
- * o: [n_rows, d] doubles (or [B,H,N,d] when rows == NULL); lse: [n_rows] or NULL.
- * n_threads <= 0 uses one thread. Returns 0 on success, -1 on bad arguments,
- * -2 when memory runs out.
+ * Computes O (and lse) for the listed query rows, or for all B*H*Nq rows when
+ * rows == NULL. q: fp16 bit patterns [B,H,Nq,d]; k, v: [B,Hkv,Nk,d], H a multiple
+ * of Hkv. key_lengths: [B] or NULL. rows: flat row ids (b*H + h)*Nq + i in
+ * ascending order, n_rows of them. o: [n_rows, d] doubles (or [B,H,Nq,d] when
+ * rows == NULL); lse: [n_rows] or NULL. n_threads <= 0 uses one thread. Returns 0
+ * on success, -1 on bad arguments, -2 when memory runs out.
  */
-int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B, int64_t H,
-                int64_t N, int64_t d, double sm_scale, int causal, const int32_t *key_lengths,
-                const int64_t *rows, int64_t n_rows, double *o, double *lse, int n_threads)
+int oracle_attn_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B, int64_t H,
+                   int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, double sm_scale, int causal,
+                   const int32_t *key_lengths, const int64_t *rows, int64_t n_rows, double *o,
+                   double *lse, int n_threads)
 {
-    if (!q || !k || !v || !o || B < 0 || H < 0 || N < 0 || d <= 0)
+    const int64_t N = Nq;
+    if (!q || !k || !v || !o || B < 0 || H < 0 || N < 0 || Nk < 0 || d <= 0 || Hkv < 1 ||
+        H % Hkv != 0)
         return -1;
     int64_t total = B * H * N;
     if (!rows)
@@ -242,6 +256,7 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t
     memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v;
     J.B = B; J.H = H; J.N = N; J.d = d;
+    J.Hkv = Hkv; J.Nk = Nk;
     J.sm_scale = sm_scale;
     J.causal = causal;
     J.key_lengths = key_lengths;
@@ -276,4 +291,13 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t
     free(begin);
     pthread_mutex_destroy(&J.lock);
     return J.failed ? -2 : 0;
+}
+
+/* Self-attention (Nq = Nk = N, Hkv = H): q, k, v all [B,H,N,d]; see oracle_attn_ex. */
+int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B, int64_t H,
+                int64_t N, int64_t d, double sm_scale, int causal, const int32_t *key_lengths,
+                const int64_t *rows, int64_t n_rows, double *o, double *lse, int n_threads)
+{
+    return oracle_attn_ex(q, k, v, B, H, H > 0 ? H : 1, N, N, d, sm_scale, causal, key_lengths,
+                          rows, n_rows, o, lse, n_threads);
 }

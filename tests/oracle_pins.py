@@ -13,6 +13,9 @@ What pins what:
   closed forms (uniform keys, one-hot selection, causal
   row 0, N = 1, d = 1 / N = 2 logistic weight)           -> masks, index order, scale
   invariances (joint permutation, score shift)            -> operand roles, lse offset
+  reductions to the self-attention case (repeated K/V
+  heads, padded Q or K/V, shifted query rows)              -> head groups, Nq != Nk, causal
+                                                              diagonal of cross-attention
 """
 from __future__ import annotations
 
@@ -295,6 +298,96 @@ def pin_row_sampling(orc):
     assert np.array_equal(lse_r, lse.reshape(-1)[rows])
 
 
+def pin_gqa_is_repeated_kv(orc):
+    """Grouped-query attention ("natural extensions" of the cuda-reranker README): query head h
+    reads key/value head h // (H // Hkv), so the result equals multi-head attention with each
+    K, V head repeated for its group of consecutive query heads."""
+    B, H, N, d = 2, 6, 13, 8
+    q = _rand((B, H, N, d), 111)
+    for Hkv in (1, 2, 3):
+        k, v = _rand((B, Hkv, N, d), 112 + Hkv), _rand((B, Hkv, N, d), 122 + Hkv)
+        kr, vr = np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1)
+        for causal in (False, True):
+            kl = np.array([13, 6], np.int32)
+            o, lse = orc.attn(q, k, v, sm_scale=0.45, causal=causal, key_lengths=kl)
+            ro, rl = orc.attn(q, kr, vr, sm_scale=0.45, causal=causal, key_lengths=kl)
+            assert np.array_equal(o, ro) and np.array_equal(lse, rl)
+    # a mapping by h % Hkv instead would differ: check the groups are not interleaved
+    k, v = _rand((B, 2, N, d), 131), _rand((B, 2, N, d), 132)
+    o, _ = orc.attn(q, k, v, sm_scale=0.45)
+    oi, _ = orc.attn(q, np.tile(k, (1, 3, 1, 1)), np.tile(v, (1, 3, 1, 1)), sm_scale=0.45)
+    assert np.max(np.abs(o - oi)) > 1e-3
+
+
+def pin_cross_is_padded_self(orc):
+    """Cross-attention (Nq != Nk) without a causal mask: every query row sees the same keys as in
+    self-attention, so the rows equal those of a self-attention problem whose Q is padded with
+    extra rows (Nq < Nk) or whose K, V are padded with rows excluded by key padding (Nq > Nk)."""
+    B, H, d = 2, 2, 8
+    for Nq, Nk in ((5, 19), (19, 5), (1, 33)):
+        q = _rand((B, H, Nq, d), 140 + Nq)
+        k, v = _rand((B, H, Nk, d), 150 + Nk), _rand((B, H, Nk, d), 160 + Nk)
+        N = max(Nq, Nk)
+        qp = np.concatenate([q, _rand((B, H, N - Nq, d), 170)], axis=2)
+        kp = np.concatenate([k, _rand((B, H, N - Nk, d), 171)], axis=2)
+        vp = np.concatenate([v, _rand((B, H, N - Nk, d), 172)], axis=2)
+        for kl in (None, np.array([Nk, max(1, Nk // 2)], np.int32)):
+            o, lse = orc.attn(q, k, v, sm_scale=0.55, key_lengths=kl)
+            klp = np.full(B, Nk, np.int32) if kl is None else kl
+            ro, rl = orc.attn(qp, kp, vp, sm_scale=0.55, key_lengths=klp)
+            assert np.array_equal(o, ro[:, :, :Nq]) and np.array_equal(lse, rl[:, :, :Nq])
+
+
+def pin_cross_causal_alignment(orc):
+    """Causal cross-attention with the diagonal at the last rows: query i sees keys
+    j <= i + Nk - Nq. For Nq < Nk the rows are the last Nq rows of self-attention over Nk keys
+    (the real queries placed at positions Nk - Nq ..). For Nq > Nk the first Nq - Nk rows see no
+    key (O = 0, lse = -inf) and the rest are self-attention of the last Nk queries."""
+    B, H, d = 2, 2, 8
+    for Nq, Nk in ((6, 21), (21, 6), (1, 17), (9, 9)):
+        q = _rand((B, H, Nq, d), 180 + Nq)
+        k, v = _rand((B, H, Nk, d), 190 + Nk), _rand((B, H, Nk, d), 200 + Nk)
+        kl = np.array([Nk, max(1, Nk - 4)], np.int32)
+        o, lse = orc.attn(q, k, v, sm_scale=0.6, causal=True, key_lengths=kl)
+        if Nq <= Nk:
+            qp = np.concatenate([_rand((B, H, Nk - Nq, d), 210), q], axis=2)
+            ro, rl = orc.attn(qp, k, v, sm_scale=0.6, causal=True, key_lengths=kl)
+            assert np.array_equal(o, ro[:, :, Nk - Nq:]) and np.array_equal(lse, rl[:, :, Nk - Nq:])
+        else:
+            e = Nq - Nk
+            assert np.all(o[:, :, :e] == 0.0) and np.all(lse[:, :, :e] == -np.inf)
+            ro, rl = orc.attn(q[:, :, e:], k, v, sm_scale=0.6, causal=True, key_lengths=kl)
+            assert np.array_equal(o[:, :, e:], ro) and np.array_equal(lse[:, :, e:], rl)
+
+
+def pin_cross_gqa_uniform_keys(orc):
+    """All key rows equal, cross-attention with groups: O_i is the mean of V over the first
+    n_i = min(L_b, i + Nk - Nq + 1) keys of the group's key/value head (the first L_b
+    keys without the causal mask), and lse_i = scale * q_i.k + ln n_i; n_i = 0 gives O = 0,
+    lse = -inf."""
+    B, H, Hkv, Nq, Nk, d = 2, 4, 2, 11, 7, 4
+    q = _rand((B, H, Nq, d), 221)
+    k = np.broadcast_to(_rand((B, Hkv, 1, d), 222), (B, Hkv, Nk, d)).copy()
+    v = _rand((B, Hkv, Nk, d), 223)
+    kl = np.array([7, 3], np.int32)
+    scale = 0.5
+    for causal in (False, True):
+        o, lse = orc.attn(q, k, v, sm_scale=scale, causal=causal, key_lengths=kl)
+        for b in range(B):
+            for h in range(H):
+                g = h // (H // Hkv)
+                for i in range(Nq):
+                    n = min(kl[b], i + Nk - Nq + 1) if causal else kl[b]
+                    n = max(n, 0)
+                    if n == 0:
+                        assert np.all(o[b, h, i] == 0.0) and lse[b, h, i] == -np.inf
+                        continue
+                    mean = v[b, g, :n].astype(np.float64).mean(axis=0)
+                    assert np.max(np.abs(o[b, h, i] - mean)) < 1e-12
+                    s = scale * float(q[b, h, i].astype(np.float64) @ k[b, g, 0].astype(np.float64))
+                    assert abs(lse[b, h, i] - (s + math.log(n))) < 1e-12
+
+
 ALL_PINS = [
     pin_half_decoder,
     pin_dot_product_golden,
@@ -310,4 +403,8 @@ ALL_PINS = [
     pin_permutation_invariance,
     pin_shift_invariance,
     pin_row_sampling,
+    pin_gqa_is_repeated_kv,
+    pin_cross_is_padded_self,
+    pin_cross_causal_alignment,
+    pin_cross_gqa_uniform_keys,
 ]

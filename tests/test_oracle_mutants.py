@@ -11,14 +11,19 @@ from oracle_pins import ALL_PINS
 
 MUTANTS = {
     "dropped_scale": ("s[j] = sm_scale * dot;", "s[j] = dot;"),
-    "causal_off_by_one": ("if (causal && j > i)", "if (causal && j >= i)"),
+    "causal_off_by_one": ("if (causal && j > i + off)", "if (causal && j >= i + off)"),
+    "causal_offset_sign": ("if (causal && j > i + off)", "if (causal && j > i - off)"),
+    "causal_top_left": ("if (causal && j > i + off)", "if (causal && j > i)"),
+    "kv_head_interleaved": ("int64_t kvh = b * J->Hkv + h / G;", "int64_t kvh = b * J->Hkv + h % J->Hkv;"),
+    "kv_head_query_stride": ("int64_t kvh = b * J->Hkv + h / G;", "int64_t kvh = b * J->H + h / G;"),
+    "length_clamp_to_nq": ("if (L > Nk) L = Nk;", "if (L > N) L = N;"),
     "padding_off_by_one": ("if (j >= L)", "if (j > L)"),
     "lse_dropped_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "no_normalisation": ("double p = exp(s[j] - m) / l;", "double p = exp(s[j] - m);"),
     "wrong_sign_exponent": ("double p = exp(s[j] - m) / l;", "double p = exp(m - s[j]) / l;"),
     "v_uses_k": ("o[c] += p * V[j * d + c];", "o[c] += p * K[j * d + c];"),
     "q_dot_v": ("dot += q[c] * K[j * d + c];", "dot += q[c] * V[j * d + c];"),
-    "normaliser_without_mask": ("if (allowed(i, j, L, causal))\n            l += exp(s[j] - m);",
+    "normaliser_without_mask": ("if (allowed(i, j, L, causal, off))\n            l += exp(s[j] - m);",
                                 "if (1)\n            l += exp(s[j] - m);"),
     "decoder_bias": ("mag = ldexp((double)(1024 + f), e - 25);", "mag = ldexp((double)(1024 + f), e - 24);"),
     "subnormal_scale": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
