@@ -6,7 +6,10 @@ forward over the whole batch with inputs resident in HBM. The same line carries:
   e2e          the same metric through the public API with host tensors (pinned host ->
                device copies of Q, K, V and the device -> host copy of O inside the timing)
   short_n      the reranking workload (B=50, H=12, N=256, d=32, key padding) in GB/s of
-               minimum traffic, L2 flushed before every timed launch
+               minimum traffic, inputs rotated over buffer sets larger than L2
+  split_kv     one long causal head, the tiled kernel alone and with split-KV
+  gqa          grouped-query prefill (32 query heads over 8 key/value heads) and a block of
+               1024 queries over 16384 cached keys, in TFLOP/s
   roofline     the dominant kernel's achieved FLOP/s against the measured peak
   cpu_baseline the fp64 oracle timed on the host cores on a bounded sample (rank 0, N=1)
   clocks       SM clocks and throttle reasons sampled during the timed region
@@ -51,6 +54,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short-n", action="store_true")
     ap.add_argument("--no-split-kv", action="store_true")
+    ap.add_argument("--no-gqa", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
 
@@ -157,7 +161,7 @@ def oracle_sample(w, q, k, v, kl, heads):
     t0 = time.perf_counter()
     oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal, key_lengths=kl, rows=rows)
     dt = time.perf_counter() - t0
-    flops = synth.attention_flops(1, len(heads), w.N, w.d, w.causal)
+    flops = synth.attention_flops_ex(1, len(heads), w.N, w.N_k, w.d, w.causal)
     return flops, dt, oracle.default_threads()
 
 
@@ -199,11 +203,15 @@ def run_reference(args):
 
 
 def workload_config(w):
-    return {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-            "causal": w.causal, "sm_scale": w.sm_scale,
-            "key_lengths": list(w.key_len_range) if w.key_len_range else None,
-            "l2": "inputs larger than L2" if synth.min_bytes(w.B, w.H, w.N, w.d) > 2 * 129e6
-            else "L2 flushed between timed launches"}
+    cfg = {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+           "causal": w.causal, "sm_scale": w.sm_scale,
+           "key_lengths": list(w.key_len_range) if w.key_len_range else None,
+           "l2": "inputs larger than L2"
+           if synth.min_bytes_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d) > 2 * 129e6
+           else "L2 flushed between timed launches"}
+    if (w.H_kv, w.N_k) != (w.H, w.N):
+        cfg.update(H_kv=w.H_kv, N_k=w.N_k)
+    return cfg
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -283,7 +291,7 @@ def main():
     qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
     kld = torch.from_numpy(kl).cuda() if kl is not None else None
     od = torch.empty_like(qd)
-    flops = synth.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    flops = synth.attention_flops_ex(w.B, w.H, w.N, w.N_k, w.d, w.causal)
 
     def step():
         api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od,
@@ -344,7 +352,9 @@ def main():
     d2h = q.nbytes
 
     # Roofline of the dominant (only) kernel.
-    kernel_name = api.auto_path(w.N, w.d) if args.path == "auto" else args.path
+    kernel_name = args.path
+    if args.path == "auto":
+        kernel_name = api.auto_path(w.N, w.d) if (w.H_kv, w.N_k) == (w.H, w.N) else "tcgen05"
     avg_launch_ms = statistics.mean(launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -369,6 +379,8 @@ def main():
         line["short_n"] = short_n(torch, api, peaks, peak_src)
     if not args.no_split_kv:
         line["split_kv"] = split_kv(torch, api, peaks, peak_src)
+    if not args.no_gqa:
+        line["gqa"] = gqa(torch, api, peaks, peak_src)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # Bounded sample of the same workload: the first heads (flat batch*head order), all
@@ -485,6 +497,36 @@ def split_kv(torch, api, peaks, peak_src):
             "roofline": {"bound": "tensor", "achieved": tf["split"], "peak": peak, "unit": "TFLOP/s",
                          "frac": tf["split"] / peak, "peak_source": f"{peak_src} bf16 dense burst"},
             "l2": "flushed (512 MiB write) before every timed launch; the split launch includes the merge kernel"}
+
+
+def gqa(torch, api, peaks, peak_src):
+    """Grouped-query and cross-attention shapes on the tiled kernel, TFLOP/s of the contract
+    count (allowed query/key pairs as the area under the causal diagonal); L2 flushed before
+    every timed launch."""
+    flush = l2_flush_buffer(torch)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    out = {}
+    for name in ("gqa_prefill", "chunk_prefill"):
+        w = synth.WORKLOADS[name]
+        q, k, v, _ = synth.draw_workload(w)
+        qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+        od = torch.empty_like(qd)
+        flops = synth.attention_flops_ex(w.B, w.H, w.N, w.N_k, w.d, w.causal)
+
+        def fn():
+            api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od)
+
+        time_launches(torch, fn, 3, flush)
+        ms = statistics.median(time_launches(torch, fn, 30, flush))
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"workload": w.describe(), "value": tf, "unit": "TFLOP/s", "launch_ms": ms,
+                     "kernel": "tcgen05",
+                     "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
+                                  "unit": "TFLOP/s", "frac": tf / peak,
+                                  "peak_source": f"{peak_src} bf16 dense burst"}}
+        del qd, kd, vd, od
+    out["l2"] = "flushed (512 MiB write) before every timed launch"
+    return out
 
 
 if __name__ == "__main__":

@@ -46,6 +46,10 @@ SIGNATURES = {
     "attn_splitkv_auto_splits": (_i, [_i, _i, _i, _i, _i]),
     "attn_fwd_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "attn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_fwd_splitkv_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp,
+                                 ctypes.c_size_t, _vp]),
+    "attn_splitkv_auto_splits_ex": (_i, [_i, _i, _i, _i, _i, _i]),
 }
 
 _lib = None

@@ -31,9 +31,11 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
         sm_scale: float | None = None, key_lengths: torch.Tensor | None = None,
         return_lse: bool = False, out: torch.Tensor | None = None,
         lse_out: torch.Tensor | None = None, path: str = "auto"):
-    """O = softmax(sm_scale * Q K^T + mask) V for fp16 [B, H, N, d] tensors.
+    """O = softmax(sm_scale * Q K^T + mask) V for fp16 tensors: q [B, H, N, d] and k, v of the
+    same shape (self-attention) or [B, H_kv, N_k, d] (cross-attention and grouped-query
+    attention: H a multiple of H_kv, query head h reads key/value head h // (H // H_kv)).
 
-    causal: key j allowed for query i only when j <= i.
+    causal: key j allowed for query i only when j <= i + N_k - N (j <= i for self-attention).
     key_lengths: int32 [B]; keys j >= key_lengths[b] are excluded.
     sm_scale: defaults to 1/sqrt(d).
     return_lse: also return the fp32 [B, H, N] logsumexp.
@@ -45,12 +47,11 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
     if q.device.type == "cpu":
         return _fwd_host(q, k, v, causal=causal, sm_scale=sm_scale, key_lengths=key_lengths,
                          return_lse=return_lse, out=out, lse_out=lse_out, path=path)
-    if q.dim() != 4:
-        raise ValueError("q must be [B, H, N, d]")
-    B, H, N, d = q.shape
+    B, H, N, d, Hkv, Nk = _shapes(q, k)
     dev = q.device
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_device_tensor(name, t, (B, H, N, d), torch.float16, dev)
+    _check_device_tensor("q", q, (B, H, N, d), torch.float16, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check_device_tensor(name, t, (B, Hkv, Nk, d), torch.float16, dev)
     if dev.type != "cuda":
         raise ValueError("tensors must be CUDA tensors (or CPU tensors for the host path)")
     if out is None:
@@ -67,16 +68,34 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
         sm_scale = 1.0 / math.sqrt(d)
     if path not in _lib.PATHS:
         raise ValueError(f"path must be one of {sorted(_lib.PATHS)}")
+    kl_ptr = key_lengths.data_ptr() if key_lengths is not None else None
+    lse_ptr = lse.data_ptr() if lse is not None else None
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-        st = _lib.lib().attn_fwd_path(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-            lse.data_ptr() if lse is not None else None, B, H, N, d, float(sm_scale),
-            int(bool(causal)), key_lengths.data_ptr() if key_lengths is not None else None,
-            _lib.PATHS[path], stream)
+        if (Hkv, Nk) == (H, N):
+            what = "attn_fwd_path"
+            st = _lib.lib().attn_fwd_path(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, N, d,
+                float(sm_scale), int(bool(causal)), kl_ptr, _lib.PATHS[path], stream)
+        else:
+            what = "attn_fwd_ex"
+            st = _lib.lib().attn_fwd_ex(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, Hkv, N, Nk,
+                d, float(sm_scale), int(bool(causal)), kl_ptr, _lib.PATHS[path], stream)
     if st != _lib.ATTN_OK:
-        raise _lib.AttnError(st, "attn_fwd_path")
+        raise _lib.AttnError(st, what)
     return (out, lse) if return_lse else out
+
+
+def _shapes(q, k):
+    """(B, H, N, d, H_kv, N_k) of q [B, H, N, d] and k [B, H_kv, N_k, d]."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, H, N, d] and k, v [B, H_kv, N_k, d]")
+    B, H, N, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d or Hkv < 1 or H % Hkv != 0:
+        raise ValueError("k, v must be [B, H_kv, N_k, d] with H a multiple of H_kv")
+    return B, H, N, d, Hkv, Nk
 
 
 def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
@@ -85,17 +104,17 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
                 lse_out: torch.Tensor | None = None, n_splits: int = 0,
                 workspace: torch.Tensor | None = None):
     """fwd() with the keys of every query tile pair split into n_splits ranges that run as
-    separate work units and are merged exactly (attn_fwd_splitkv). n_splits <= 0 chooses the
-    count for the current device. workspace: a CUDA tensor of at least
-    splitkv_workspace_bytes(...) bytes (allocated here when None). Device tensors only."""
-    if q.dim() != 4:
-        raise ValueError("q must be [B, H, N, d]")
-    B, H, N, d = q.shape
+    separate work units and are merged exactly (attn_fwd_splitkv, attn_fwd_splitkv_ex for
+    k, v of another shape than q). n_splits <= 0 chooses the count for the current device.
+    workspace: a CUDA tensor of at least splitkv_workspace_bytes(...) bytes (allocated here
+    when None). Device tensors only."""
+    B, H, N, d, Hkv, Nk = _shapes(q, k)
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("fwd_splitkv takes CUDA tensors")
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_device_tensor(name, t, (B, H, N, d), torch.float16, dev)
+    _check_device_tensor("q", q, (B, H, N, d), torch.float16, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check_device_tensor(name, t, (B, Hkv, Nk, d), torch.float16, dev)
     if out is None:
         out = torch.empty_like(q)
     _check_device_tensor("out", out, (B, H, N, d), torch.float16, dev)
@@ -111,7 +130,7 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
     L = _lib.lib()
     with torch.cuda.device(dev):
         if n_splits <= 0:
-            n_splits = L.attn_splitkv_auto_splits(B, H, N, d, int(bool(causal)))
+            n_splits = L.attn_splitkv_auto_splits_ex(B, H, N, Nk, d, int(bool(causal)))
         need = L.attn_splitkv_workspace_bytes(B, H, N, d, int(n_splits))
         if need == 0:
             raise ValueError(f"invalid split-KV sizes (n_splits={n_splits})")
@@ -120,14 +139,23 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
         if workspace.device != dev or not workspace.is_contiguous():
             raise ValueError("workspace must be a contiguous tensor on the device of q")
         stream = torch.cuda.current_stream(dev).cuda_stream
-        st = L.attn_fwd_splitkv(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-            lse.data_ptr() if lse is not None else None, B, H, N, d, float(sm_scale),
-            int(bool(causal)), key_lengths.data_ptr() if key_lengths is not None else None,
-            int(n_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-            stream)
+        lse_ptr = lse.data_ptr() if lse is not None else None
+        kl_ptr = key_lengths.data_ptr() if key_lengths is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size()
+        if (Hkv, Nk) == (H, N):
+            what = "attn_fwd_splitkv"
+            st = L.attn_fwd_splitkv(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, N, d,
+                float(sm_scale), int(bool(causal)), kl_ptr, int(n_splits), workspace.data_ptr(),
+                ws_bytes, stream)
+        else:
+            what = "attn_fwd_splitkv_ex"
+            st = L.attn_fwd_splitkv_ex(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, Hkv, N,
+                Nk, d, float(sm_scale), int(bool(causal)), kl_ptr, int(n_splits),
+                workspace.data_ptr(), ws_bytes, stream)
     if st != _lib.ATTN_OK:
-        raise _lib.AttnError(st, "attn_fwd_splitkv")
+        raise _lib.AttnError(st, what)
     return (out, lse) if return_lse else out
 
 

@@ -40,24 +40,31 @@ cudaError_t status_word(unsigned int **out)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Sizes of one call: H query heads of N_q rows, H_kv key/value heads of N_k keys.
+struct Shape {
+    int B, H, Hkv, Nq, Nk, d;
+    bool self() const { return Hkv == H && Nq == Nk; }
+};
+
 attn_status_t validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                       int B, int H, int N, int d, float sm_scale, int causal,
-                       const int32_t *key_lengths)
+                       const Shape &sh, float sm_scale, int causal, const int32_t *key_lengths)
 {
     if (!q || !k || !v || !o)
         return ATTN_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1)
+    if (sh.B < 1 || sh.H < 1 || sh.Hkv < 1 || sh.Nq < 1 || sh.Nk < 1 || sh.H % sh.Hkv != 0)
         return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1)
         return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(sm_scale))
         return ATTN_ERR_INVALID_ARG;
-    if (d != 32 && d != 64 && d != 128)
+    if (sh.d != 32 && sh.d != 64 && sh.d != 128)
         return ATTN_ERR_UNSUPPORTED;
-    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int64_t bh = static_cast<int64_t>(sh.B) * sh.H;
     if (bh > INT32_MAX)
         return ATTN_ERR_INVALID_ARG;
-    if (bh * N > INT64_MAX / d) // element count of one tensor must fit int64
+    const int64_t bhkv = static_cast<int64_t>(sh.B) * sh.Hkv;
+    // element count of every tensor must fit int64
+    if (bh * sh.Nq > INT64_MAX / sh.d || bhkv * sh.Nk > INT64_MAX / sh.d)
         return ATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
         return ATTN_ERR_MISALIGNED;
@@ -65,6 +72,37 @@ attn_status_t validate(const void *q, const void *k, const void *v, const void *
         return ATTN_ERR_MISALIGNED;
     return ATTN_OK;
 }
+
+attn::FwdParams make_params(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const Shape &sh, float sm_scale, int causal, const int32_t *key_lengths)
+{
+    attn::FwdParams p;
+    p.q = static_cast<const __half *>(q);
+    p.k = static_cast<const __half *>(k);
+    p.v = static_cast<const __half *>(v);
+    p.o = static_cast<__half *>(o);
+    p.lse = lse;
+    p.key_lengths = key_lengths;
+    p.B = sh.B;
+    p.H = sh.H;
+    p.N = sh.Nq;
+    p.d = sh.d;
+    p.Hkv = sh.Hkv;
+    p.Nk = sh.Nk;
+    p.sm_scale = sm_scale;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.causal = causal;
+    p.wait_limit_ns = attn::kDefaultWaitLimitNs;
+    p.inject_missing_arrive = 0;
+    return p;
+}
+
+Shape self_shape(int B, int H, int N, int d) { return Shape{B, H, H, N, N, d}; }
+
+// One forward pass on the chosen kernel (the automatic choice when path is ATTN_PATH_AUTO).
+attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh,
+                      float sm_scale, int causal, const int32_t *key_lengths, int path,
+                      const attn_debug_opts_t *opts, attn_stream_t stream);
 
 } // namespace
 
@@ -93,37 +131,27 @@ extern "C" int attn_auto_path(int N, int d)
     return ATTN_PATH_TCGEN05;
 }
 
-extern "C" attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *o,
-                                        float *lse, int B, int H, int N, int d, float sm_scale,
-                                        int causal, const int32_t *key_lengths, int path,
-                                        const attn_debug_opts_t *opts, attn_stream_t stream)
+namespace {
+
+attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh,
+                      float sm_scale, int causal, const int32_t *key_lengths, int path,
+                      const attn_debug_opts_t *opts, attn_stream_t stream)
 {
-    attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
+    attn_status_t st = validate(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
         return st;
     if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
         path != ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
-    if (path == ATTN_PATH_SHORT && (N > 256 || d > 64))
+    // The short-sequence kernel serves self-attention only.
+    if (path == ATTN_PATH_SHORT && (!sh.self() || sh.Nq > 256 || sh.d > 64))
         return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_AUTO)
-        path = attn_auto_path(N, d);
+        path = sh.self() ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;
 
-    attn::FwdParams p;
-    p.q = static_cast<const __half *>(q);
-    p.k = static_cast<const __half *>(k);
-    p.v = static_cast<const __half *>(v);
-    p.o = static_cast<__half *>(o);
-    p.lse = lse;
-    p.key_lengths = key_lengths;
-    p.B = B;
-    p.H = H;
-    p.N = N;
-    p.d = d;
-    p.sm_scale = sm_scale;
-    p.scale_log2 = sm_scale * 1.4426950408889634f;
-    p.causal = causal;
-    p.wait_limit_ns = (opts && opts->wait_limit_ns) ? opts->wait_limit_ns : attn::kDefaultWaitLimitNs;
+    attn::FwdParams p = make_params(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
+    if (opts && opts->wait_limit_ns)
+        p.wait_limit_ns = opts->wait_limit_ns;
     p.inject_missing_arrive = opts ? (opts->inject_missing_arrive != 0) : 0;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -138,6 +166,26 @@ extern "C" attn_status_t attn_fwd_debug(const void *q, const void *k, const void
         err = attn::launch_warp_mma(p, s);
     }
     return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *o,
+                                        float *lse, int B, int H, int N, int d, float sm_scale,
+                                        int causal, const int32_t *key_lengths, int path,
+                                        const attn_debug_opts_t *opts, attn_stream_t stream)
+{
+    return run_fwd(q, k, v, o, lse, self_shape(B, H, N, d), sm_scale, causal, key_lengths, path, opts,
+                   stream);
+}
+
+extern "C" attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                     int B, int H, int H_kv, int N_q, int N_k, int d, float sm_scale,
+                                     int causal, const int32_t *key_lengths, int path,
+                                     attn_stream_t stream)
+{
+    return run_fwd(q, k, v, o, lse, Shape{B, H, H_kv, N_q, N_k, d}, sm_scale, causal, key_lengths, path,
+                   nullptr, stream);
 }
 
 extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,
@@ -187,13 +235,28 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S)
 
 // Ranges per (batch*head, Q tile pair) for the automatic choice: enough (pair, range) units
 // that the largest one is no longer than an SM's average share. Without a causal mask every
-// pair has the same work and one unit per SM suffices; with it the largest pair has about
-// twice the average. At most one range per two K/V tiles, at most kMaxSplits.
-int auto_splits(int B, int H, int N, int causal, int sms)
+// pair has the same work and one unit per SM suffices; with it the largest pair has
+// (max / mean) of the pairs' K/V tile counts times the average (about 2 for self-attention).
+// At most one range per two K/V tiles, at most kMaxSplits.
+int auto_splits(int B, int H, int Nq, int Nk, int causal, int sms)
 {
-    const long long pairs = static_cast<long long>(B) * H * ((N + 255) / 256);
-    const long long want = (static_cast<long long>(sms) * (causal ? 2 : 1) + pairs - 1) / pairs;
-    const int kv_tiles = (N + 127) / 128;
+    const int n_pairs = (Nq + 255) / 256;
+    const long long pairs = static_cast<long long>(B) * H * n_pairs;
+    double skew = 1.0;
+    if (causal) {
+        long long sum = 0, mx = 0;
+        for (int pr = 0; pr < n_pairs; ++pr) {
+            long long e = static_cast<long long>(pr) * 256 + 256 + Nk - Nq;
+            e = e < 0 ? 0 : (e > Nk ? Nk : e);
+            const long long f = (e + 127) / 128;
+            sum += f;
+            mx = f > mx ? f : mx;
+        }
+        if (sum > 0)
+            skew = static_cast<double>(mx) * n_pairs / static_cast<double>(sum);
+    }
+    const long long want = static_cast<long long>(std::ceil(static_cast<double>(sms) * skew / pairs));
+    const int kv_tiles = (Nk + 127) / 128;
     long long s = want < 1 ? 1 : want;
     if (s > kv_tiles / 2)
         s = kv_tiles / 2;
@@ -209,14 +272,54 @@ extern "C" size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n
     return splitkv_bytes(B, H, N, d, n_splits);
 }
 
-extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal)
+extern "C" int attn_splitkv_auto_splits_ex(int B, int H, int N_q, int N_k, int d, int causal)
 {
-    if (B < 1 || H < 1 || N < 1 || (d != 32 && d != 64 && d != 128) || (causal != 0 && causal != 1))
+    if (B < 1 || H < 1 || N_q < 1 || N_k < 1 || (d != 32 && d != 64 && d != 128) ||
+        (causal != 0 && causal != 1))
         return -1;
     int sms = 0;
     if (attn::device_sm_count(&sms) != cudaSuccess || sms < 1)
         sms = 148;
-    return auto_splits(B, H, N, causal, sms);
+    return auto_splits(B, H, N_q, N_k, causal, sms);
+}
+
+extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal)
+{
+    return attn_splitkv_auto_splits_ex(B, H, N, N, d, causal);
+}
+
+extern "C" attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, void *o,
+                                             float *lse, int B, int H, int H_kv, int N_q, int N_k, int d,
+                                             float sm_scale, int causal, const int32_t *key_lengths,
+                                             int n_splits, void *workspace, size_t workspace_bytes,
+                                             attn_stream_t stream)
+{
+    const Shape sh{B, H, H_kv, N_q, N_k, d};
+    attn_status_t st = validate(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
+    if (st != ATTN_OK)
+        return st;
+    if (n_splits <= 0) {
+        n_splits = attn_splitkv_auto_splits_ex(B, H, N_q, N_k, d, causal);
+        if (n_splits < 1)
+            return ATTN_ERR_INVALID_ARG;
+    }
+    if (n_splits > kMaxSplits)
+        return ATTN_ERR_INVALID_ARG;
+    const size_t need = splitkv_bytes(B, H, N_q, d, n_splits);
+    if (need == 0 || !workspace || workspace_bytes < need)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16))
+        return ATTN_ERR_MISALIGNED;
+    attn::FwdParams p = make_params(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
+    unsigned int *status = nullptr;
+    cudaError_t err = status_word(&status);
+    if (err != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    float *opart = static_cast<float *>(workspace);
+    float *lpart = opart + static_cast<size_t>(n_splits) * B * H * N_q * d;
+    err = attn::launch_tcgen05_splitkv(p, n_splits, opart, lpart, reinterpret_cast<cudaStream_t>(stream),
+                                       status);
+    return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -224,46 +327,8 @@ extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const vo
                                           const int32_t *key_lengths, int n_splits, void *workspace,
                                           size_t workspace_bytes, attn_stream_t stream)
 {
-    attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
-    if (st != ATTN_OK)
-        return st;
-    if (n_splits <= 0) {
-        n_splits = attn_splitkv_auto_splits(B, H, N, d, causal);
-        if (n_splits < 1)
-            return ATTN_ERR_INVALID_ARG;
-    }
-    if (n_splits > kMaxSplits)
-        return ATTN_ERR_INVALID_ARG;
-    const size_t need = splitkv_bytes(B, H, N, d, n_splits);
-    if (need == 0 || !workspace || workspace_bytes < need)
-        return ATTN_ERR_INVALID_ARG;
-    if (!aligned(workspace, 16))
-        return ATTN_ERR_MISALIGNED;
-    attn::FwdParams p;
-    p.q = static_cast<const __half *>(q);
-    p.k = static_cast<const __half *>(k);
-    p.v = static_cast<const __half *>(v);
-    p.o = static_cast<__half *>(o);
-    p.lse = lse;
-    p.key_lengths = key_lengths;
-    p.B = B;
-    p.H = H;
-    p.N = N;
-    p.d = d;
-    p.sm_scale = sm_scale;
-    p.scale_log2 = sm_scale * 1.4426950408889634f;
-    p.causal = causal;
-    p.wait_limit_ns = attn::kDefaultWaitLimitNs;
-    p.inject_missing_arrive = 0;
-    unsigned int *status = nullptr;
-    cudaError_t err = status_word(&status);
-    if (err != cudaSuccess)
-        return ATTN_ERR_CUDA;
-    float *opart = static_cast<float *>(workspace);
-    float *lpart = opart + static_cast<size_t>(n_splits) * B * H * N * d;
-    err = attn::launch_tcgen05_splitkv(p, n_splits, opart, lpart, reinterpret_cast<cudaStream_t>(stream),
-                                       status);
-    return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return attn_fwd_splitkv_ex(q, k, v, o, lse, B, H, H, N, N, d, sm_scale, causal, key_lengths, n_splits,
+                               workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- split-KV without allocation
@@ -316,7 +381,7 @@ extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void *q, const void *k, 
                                                   int causal, const int32_t *key_lengths, int n_splits,
                                                   attn_stream_t stream)
 {
-    attn_status_t st = validate(q, k, v, o, lse, B, H, N, d, sm_scale, causal, key_lengths);
+    attn_status_t st = validate(q, k, v, o, lse, self_shape(B, H, N, d), sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
         return st;
     if (n_splits <= 0) {

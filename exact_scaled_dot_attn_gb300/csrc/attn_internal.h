@@ -14,7 +14,10 @@ struct FwdParams {
     __half *o;
     float *lse;                 // may be null
     const int32_t *key_lengths; // may be null
-    int B, H, N, d;
+    int B, H, N, d; // N: query rows per head
+    int Hkv, Nk;    // key/value heads per batch (H a multiple of Hkv) and keys per head;
+                    // self-attention: Hkv = H, Nk = N. Query head h reads key/value head
+                    // h / (H / Hkv); under the causal mask query i sees keys j <= i + Nk - N.
     float sm_scale;
     float scale_log2; // sm_scale * log2(e): scores are exponentiated with exp2
     int causal;
@@ -37,7 +40,7 @@ cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int
 cudaError_t launch_tcgen05_splitkv(const FwdParams &p, int n_splits, float *opart, float *lpart,
                                    cudaStream_t stream, unsigned int *status);
 
-// Persistent short-sequence kernel (N <= 256, d in {32, 64}).
+// Persistent short-sequence kernel (self-attention only: Nk = N <= 256, Hkv = H, d in {32, 64}).
 cudaError_t launch_short(const FwdParams &p, cudaStream_t stream, unsigned int *status);
 
 // Multiprocessor count of the current device (cached per device).

@@ -9,6 +9,9 @@
 //               whose K/V fit comfortably in L2, and inside a block the units go
 //               heaviest-first (last query rows first under a causal mask) in a snake
 //               over the CTAs, so causal triangles spread evenly without any counter.
+//               Cross-attention and grouped-query attention (the README's "natural
+//               extensions"): Q tiles are rows of a query head, K/V tiles come from
+//               its key/value head, and the causal diagonal moves by Nk - N.
 //   warp 8      TMA producer: Q0/Q1 once per unit, then K_j and V_j through a ring of
 //               shared-memory stages (full/empty mbarriers with transaction counts).
 //               K/V tiles past the causal diagonal or past key_lengths[b] are never
@@ -152,6 +155,7 @@ struct TcArgs {
 
 struct Unit {
     int bh, b, q0, L;
+    int kvh;        // key/value head (batch * Hkv + h / (H / Hkv))
     int n_kv;       // K/V tiles loaded for the unit (the larger of the two tile counts)
     int n_kv_t[2];  // K/V tiles Q tile t attends to (0 when the tile lies past N)
     int j0;         // first K/V tile of the unit's key range (split-KV; 0 otherwise)
@@ -185,17 +189,20 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
     const int pair = a.n_pairs - 1 - w / hb; // the last query rows carry the most causal work
     U.bh = h0 + w % hb;
     U.b = U.bh / a.p.H;
+    U.kvh = U.b * a.p.Hkv + (U.bh - U.b * a.p.H) / (a.p.H / a.p.Hkv);
     U.q0 = pair * 2 * kBM;
-    int L = a.p.N;
+    int L = a.p.Nk;
     if (a.p.key_lengths) {
         L = __ldg(a.p.key_lengths + U.b);
-        L = L < 0 ? 0 : (L > a.p.N ? a.p.N : L);
+        L = L < 0 ? 0 : (L > a.p.Nk ? a.p.Nk : L);
     }
     U.L = L;
     int kv_end0 = L, kv_end1 = L;
     if (a.p.causal) {
-        kv_end0 = min(L, U.q0 + kBM); // Q tile 0 stops at its own diagonal
-        kv_end1 = min(L, U.q0 + 2 * kBM);
+        // Q tile 0 stops at its own diagonal (query i sees keys j <= i + Nk - N)
+        const int off = a.p.Nk - a.p.N;
+        kv_end0 = max(0, min(L, U.q0 + kBM + off));
+        kv_end1 = max(0, min(L, U.q0 + 2 * kBM + off));
     }
     const int full0 = (kv_end0 + kBN - 1) / kBN;
     const int full1 = U.q0 + kBM < a.p.N ? (kv_end1 + kBN - 1) / kBN : 0;
@@ -562,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int bx = 0; bx < D / C::kBoxCols; ++bx)
                             tma_load_3d(sKV + slot * C::kTileBytes + bx * C::kBoxBytes,
                                         kv == 0 ? &tm_k : &tm_v, bar(BB::kKVFull + slot),
-                                        bx * C::kBoxCols, (U.j0 + j) * kBN, U.bh);
+                                        bx * C::kBoxCols, (U.j0 + j) * kBN, U.kvh);
                     }
                     __syncwarp();
                     ++kv_it;
@@ -757,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tS = lane_base + (t ? C::kTmemS1 : C::kTmemS0);
         const float scale = p.scale_log2;
+        const int diag = p.Nk - p.N; // causal: query i sees keys j <= i + diag
         uint32_t s_it = 0;
         uint32_t pv_par = 0; // bit b: parity of the PV products committed into O buffer b
         uint32_t ucnt = 0;   // units in which this tile took part
@@ -879,10 +887,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++s_it;
                 tc_fence_after();
                 const int kv0 = (U.j0 + j) * kBN;
-                const bool need_mask = (kv0 + kBN > U.L) || (p.causal && kv0 + kBN - 1 > tile_row0);
+                const bool need_mask = (kv0 + kBN > U.L) || (p.causal && kv0 + kBN - 1 > tile_row0 + diag);
                 int lim = U.L - kv0; // keys [kv0, kv0 + lim) are allowed for this row
                 if (p.causal)
-                    lim = min(lim, row - kv0 + 1);
+                    lim = min(lim, row + diag - kv0 + 1);
 
                 uint32_t sv[kBN];
                 tmem_ld128(tS, sv);
@@ -966,9 +974,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// [B*H, N, D] fp16 viewed as a 3-D tensor (D innermost); boxes of 128 rows x 64 columns
-// with a 128-byte swizzle (x 32 columns with a 64-byte swizzle for D = 32); rows past N
-// read as zero.
+// [heads, rows, D] fp16 viewed as a 3-D tensor (D innermost): Q is [B*H, N, D], K and V
+// [B*Hkv, Nk, D]; boxes of 128 rows x 64 columns with a 128-byte swizzle (x 32 columns with
+// a 64-byte swizzle for D = 32); rows past the end read as zero.
 bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
 {
     auto enc = tensor_map_encoder();
@@ -987,11 +995,12 @@ bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
 }
 
 // Heads per block of the unit order: keep the K/V of the heads in flight within about
-// 48 MB of L2, so the query-tile pairs of one head reuse its K/V from L2.
-int head_block_for(int BH, int N, int D)
+// 48 MB of L2, so the query-tile pairs of one head reuse its K/V from L2. G consecutive
+// query heads share one K/V head.
+int head_block_for(int BH, int Nk, int D, int G)
 {
-    const long long kv_head = 4LL * N * D; // K and V of one head, fp16
-    const long long hblk = (48LL << 20) / (kv_head > 0 ? kv_head : 1);
+    const long long kv_head = 4LL * Nk * D; // K and V of one key/value head, fp16
+    const long long hblk = (48LL << 20) / (kv_head > 0 ? kv_head : 1) * G;
     return static_cast<int>(hblk < 1 ? 1 : (hblk > BH ? BH : hblk));
 }
 
@@ -999,9 +1008,9 @@ int head_block_for(int BH, int N, int D)
 // the device's unit order (head block by head block, heaviest pair first inside a
 // block, the key ranges of a pair next to each other), so every CTA works on the same head
 // block at about the same time. The weight of a unit is its count of (Q tile, K/V tile)
-// steps plus a fixed per-unit cost; key lengths are not known on the host and are taken as N.
-void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, int n_pairs, int n_splits,
-                    int grid)
+// steps plus a fixed per-unit cost; key lengths are not known on the host and are taken as Nk.
+void build_schedule(SchedTable &t, int BH, int N, int Nk, int causal, int head_block, int n_pairs,
+                    int n_splits, int grid)
 {
     const int S = n_splits;
     const int n_units = BH * n_pairs * S;
@@ -1019,10 +1028,10 @@ void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, in
         const int hb = std::min(head_block, BH - blk * head_block);
         const int pair = n_pairs - 1 - w / hb;
         const int q0 = pair * 2 * kBM;
-        int e0 = N, e1 = N;
+        int e0 = Nk, e1 = Nk;
         if (causal) {
-            e0 = std::min(N, q0 + kBM);
-            e1 = std::min(N, q0 + 2 * kBM);
+            e0 = std::max(0, std::min(Nk, q0 + kBM + Nk - N));
+            e1 = std::max(0, std::min(Nk, q0 + 2 * kBM + Nk - N));
         }
         const int f0 = (e0 + kBN - 1) / kBN;
         const int f1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
@@ -1046,15 +1055,15 @@ void build_schedule(SchedTable &t, int BH, int N, int causal, int head_block, in
     t.off[grid] = static_cast<uint16_t>(k);
 }
 
-// Schedules are cached per shape (they depend on B*H, N, d, causal, the split count and the
-// SM count only).
+// Schedules are cached per shape (they depend on B*H, N, Nk, the head block, causal, the
+// split count and the SM count only).
 std::mutex g_sched_mutex;
-std::map<std::tuple<int, int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
+std::map<std::tuple<int, int, int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
 
-std::shared_ptr<SchedTable> schedule_for(int BH, int N, int D, int causal, int head_block, int n_pairs,
+std::shared_ptr<SchedTable> schedule_for(int BH, int N, int Nk, int causal, int head_block, int n_pairs,
                                          int n_splits, int grid)
 {
-    auto key = std::make_tuple(BH, N, D, causal, n_splits, grid);
+    auto key = std::make_tuple(BH, N, Nk, causal, head_block, n_splits, grid);
     std::lock_guard<std::mutex> lock(g_sched_mutex);
     auto it = g_sched_cache.find(key);
     if (it != g_sched_cache.end())
@@ -1063,7 +1072,7 @@ std::shared_ptr<SchedTable> schedule_for(int BH, int N, int D, int causal, int h
     memset(t.get(), 0, sizeof(SchedTable));
     const long long n_units = static_cast<long long>(BH) * n_pairs * n_splits;
     if (grid <= kMaxCtas && n_units <= kMaxSchedUnits)
-        build_schedule(*t, BH, N, causal, head_block, n_pairs, n_splits, grid);
+        build_schedule(*t, BH, N, Nk, causal, head_block, n_pairs, n_splits, grid);
     if (g_sched_cache.size() >= 64)
         g_sched_cache.clear();
     g_sched_cache[key] = t;
@@ -1076,9 +1085,12 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
 {
     using C = Cfg<D>;
     const int BH = p.B * p.H;
+    if (p.Hkv < 1 || p.H % p.Hkv != 0)
+        return cudaErrorInvalidValue;
+    const int BHkv = p.B * p.Hkv;
     CUtensorMap mq, mk, mv;
-    if (!encode_map(&mq, p.q, BH, p.N, D) || !encode_map(&mk, p.k, BH, p.N, D) ||
-        !encode_map(&mv, p.v, BH, p.N, D))
+    if (!encode_map(&mq, p.q, BH, p.N, D) || !encode_map(&mk, p.k, BHkv, p.Nk, D) ||
+        !encode_map(&mv, p.v, BHkv, p.Nk, D))
         return cudaErrorInvalidValue;
     TcArgs a;
     a.p = p;
@@ -1087,7 +1099,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
     if (units > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     a.n_units = static_cast<int>(units);
-    a.head_block = head_block_for(BH, p.N, D);
+    a.head_block = head_block_for(BH, p.Nk, D, p.H / p.Hkv);
     a.n_splits = n_splits;
     a.opart = opart;
     a.lpart = lpart;
@@ -1109,7 +1121,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
         return cudaErrorInvalidConfiguration;
     const int grid = a.n_units < sms ? a.n_units : sms;
     std::shared_ptr<SchedTable> sched =
-        schedule_for(BH, p.N, D, p.causal, a.head_block, a.n_pairs, n_splits, grid);
+        schedule_for(BH, p.N, p.Nk, p.causal, a.head_block, a.n_pairs, n_splits, grid);
     kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
     return cudaGetLastError();
 }

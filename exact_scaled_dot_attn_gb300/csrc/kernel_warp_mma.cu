@@ -9,6 +9,8 @@
 // never reaches memory. The causal block skip of "Engineering Decisions &
 // Trade-offs" and the all-padding tile skip of the "cuda-reranker" README both
 // reduce to stopping the tile loop at the last tile that holds an allowed key.
+// Cross-attention and grouped-query attention: the K/V rows come from the query
+// head's key/value head (Nk keys), and the causal diagonal moves by Nk - N.
 //
 // This kernel serves every head dimension and length; it is the path for short
 // sequences and d = 32, where the work is bound by memory traffic, not by the
@@ -44,40 +46,43 @@ __global__ void __launch_bounds__(kThreads)
     const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.x / BH);
     const int bh = static_cast<int>(blockIdx.x % BH);
     const int b = bh / p.H;
-    const int N = p.N;
+    const int N = p.N, Nk = p.Nk;
+    const int diag = Nk - N; // causal: query i sees keys j <= i + diag
     const int q0 = qt * kBM;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    int L = N;
+    int L = Nk;
     if (p.key_lengths) {
         L = p.key_lengths[b];
-        L = L < 0 ? 0 : (L > N ? N : L);
+        L = L < 0 ? 0 : (L > Nk ? Nk : L);
     }
     int kv_end = L;
     if (p.causal)
-        kv_end = min(kv_end, q0 + kBM);
+        kv_end = max(0, min(kv_end, q0 + kBM + diag));
     const int n_tiles = (kv_end + kBN - 1) / kBN;
 
     const size_t head_off = static_cast<size_t>(bh) * N * D;
+    const int kvh = b * p.Hkv + (bh - b * p.H) / (p.H / p.Hkv);
+    const size_t kv_off = static_cast<size_t>(kvh) * Nk * D;
     const __half *gQ = p.q + head_off;
-    const __half *gK = p.k + head_off;
-    const __half *gV = p.v + head_off;
+    const __half *gK = p.k + kv_off;
+    const __half *gV = p.v + kv_off;
 
-    // Rows [r0, r0 + rows) of one head into a swizzled tile; rows >= N are zero-filled.
-    auto load_tile = [&](__half *s, const __half *g, int r0, int rows) {
+    // Rows [r0, r0 + rows) of one head into a swizzled tile; rows >= n are zero-filled.
+    auto load_tile = [&](__half *s, const __half *g, int r0, int rows, int n) {
         for (int c = tid; c < rows * CPR; c += kThreads) {
             const int r = c / CPR, ch = c % CPR;
             const int gr = r0 + r;
-            const bool ok = gr < N;
+            const bool ok = gr < n;
             const __half *src = g + static_cast<size_t>(ok ? gr : 0) * D + ch * 8;
             cp_async16(s + swz<D>(r, ch), src, ok);
         }
     };
 
-    load_tile(sQ, gQ, q0, kBM);
+    load_tile(sQ, gQ, q0, kBM, N);
     if (n_tiles > 0) {
-        load_tile(sK, gK, 0, kBN);
-        load_tile(sV, gV, 0, kBN);
+        load_tile(sK, gK, 0, kBN, Nk);
+        load_tile(sV, gV, 0, kBN, Nk);
     }
     cp_async_commit();
 
@@ -90,8 +95,8 @@ __global__ void __launch_bounds__(kThreads)
     for (int t = 0; t < n_tiles; ++t) {
         const int st = t & 1;
         if (t + 1 < n_tiles) {
-            load_tile(sK + (st ^ 1) * kBN * D, gK, (t + 1) * kBN, kBN);
-            load_tile(sV + (st ^ 1) * kBN * D, gV, (t + 1) * kBN, kBN);
+            load_tile(sK + (st ^ 1) * kBN * D, gK, (t + 1) * kBN, kBN, Nk);
+            load_tile(sV + (st ^ 1) * kBN * D, gV, (t + 1) * kBN, kBN, Nk);
             cp_async_commit();
             cp_async_wait<1>();
         } else {
@@ -101,9 +106,10 @@ __global__ void __launch_bounds__(kThreads)
         if (t == 0)
             w.load_q(sQ, wrow0, lane);
         const int kv0 = t * kBN;
-        const bool need_mask = (kv0 + kBN > L) || (p.causal && kv0 + kBN - 1 > q0 + wrow0);
-        w.tile(sK + st * kBN * D, sV + st * kBN * D, kv0, L, p.causal != 0, need_mask, row_a, row_b,
-               p.scale_log2, lane);
+        const bool need_mask = (kv0 + kBN > L) || (p.causal && kv0 + kBN - 1 > q0 + wrow0 + diag);
+        // the masks compare keys with the diagonal column of each row: row + diag
+        w.tile(sK + st * kBN * D, sV + st * kBN * D, kv0, L, p.causal != 0, need_mask, row_a + diag,
+               row_b + diag, p.scale_log2, lane);
         __syncthreads();
     }
     cp_async_wait<0>();
@@ -116,6 +122,8 @@ __global__ void __launch_bounds__(kThreads)
 
 template <int D> cudaError_t launch_d(const FwdParams &p, cudaStream_t stream)
 {
+    if (p.Hkv < 1 || p.H % p.Hkv != 0)
+        return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(kBM * D + 4 * kBN * D) * sizeof(__half);
     cudaError_t err = cudaFuncSetAttribute(attn_fwd_warp_mma_kernel<D>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -110,7 +110,8 @@ template <int D> struct WarpRows {
 
     // One 64-key tile: k_s / v_s point at the tile's first row (a multiple of 8 rows into
     // a swizzled buffer). kv0: index of its first key; keys >= L, and keys > row under a
-    // causal mask, are excluded when need_mask is set. row_a / row_b: this thread's rows.
+    // causal mask, are excluded when need_mask is set. row_a / row_b: the last key column
+    // the causal mask allows for this thread's two rows (the row index plus Nk - N).
     __device__ __forceinline__ void tile(const __half *k_s, const __half *v_s, int kv0, int L,
                                          bool causal, bool need_mask, int row_a, int row_b,
                                          float scale_log2, int lane)

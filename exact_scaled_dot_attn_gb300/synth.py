@@ -8,7 +8,9 @@ Recipe (one numpy PCG64 stream per workload, seeded with the workload's seed):
   Q ~ N(0, sigma_qk^2), then K ~ N(0, sigma_qk^2), then V ~ N(0, sigma_v^2),
   each drawn as float32 standard normals times sigma and rounded to fp16
   (round-to-nearest-even), shape [B, H, N, d]; then, for padded workloads,
-  key_lengths[b] ~ uniform integer in [lo, hi] (inclusive).
+  key_lengths[b] ~ uniform integer in [lo, hi] (inclusive). Cross-attention and
+  grouped-query workloads draw Q as [B, H, N, d] and K, V as [B, H_kv, N_k, d] in the
+  same order.
 
 The shapes are the workloads the method is measured on: a tiny exact check, a
 cross-encoder reranking batch (the "cuda-reranker" README's shape class: many
@@ -40,6 +42,16 @@ class Workload:
     key_len_range: tuple[int, int] | None = None  # inclusive [lo, hi] when padded
     check_lse: bool = False
     ignore_padded_queries: bool = False
+    Hkv: int | None = None  # key/value heads (None: H, multi-head attention)
+    Nk: int | None = None   # keys per head (None: N, self-attention)
+
+    @property
+    def H_kv(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
+
+    @property
+    def N_k(self) -> int:
+        return self.N if self.Nk is None else self.Nk
 
     @property
     def sm_scale(self) -> float:
@@ -49,7 +61,12 @@ class Workload:
         mask = "causal" if self.causal else "no mask"
         if self.key_len_range:
             mask = f"key padding L~U[{self.key_len_range[0]},{self.key_len_range[1]}]"
-        return f"{self.name} B={self.B} H={self.H} N={self.N} d={self.d} {mask}"
+        kv = ""
+        if self.H_kv != self.H:
+            kv += f" H_kv={self.H_kv}"
+        if self.N_k != self.N:
+            kv += f" N_k={self.N_k}"
+        return f"{self.name} B={self.B} H={self.H} N={self.N}{kv} d={self.d} {mask}"
 
 
 WORKLOADS = {
@@ -62,6 +79,11 @@ WORKLOADS = {
     # one long causal sequence of a single head: fewer query tile pairs than SMs (the case the
     # split-KV path is for)
     "one_head": Workload("one_head", 1, 1, 32768, 128, True, seed=6),
+    # grouped-query prefill: 32 query heads sharing 8 key/value heads
+    "gqa_prefill": Workload("gqa_prefill", 4, 32, 4096, 128, True, seed=7, Hkv=8),
+    # a block of 1024 new queries over a cached context of 16384 keys (cross-attention shape,
+    # causal diagonal at the last rows), grouped-query heads
+    "chunk_prefill": Workload("chunk_prefill", 2, 32, 1024, 128, True, seed=8, Hkv=8, Nk=16384),
 }
 
 
@@ -87,7 +109,33 @@ def draw(B: int, H: int, N: int, d: int, seed: int, *, sigma_qk: float = 1.0,
     return q, k, v, kl
 
 
+def draw_ex(B: int, H: int, Hkv: int, N: int, Nk: int, d: int, seed: int, *,
+            sigma_qk: float = 1.0, sigma_v: float = 1.0,
+            key_len_range: tuple[int, int] | None = None):
+    """Returns (q, k, v, key_lengths): q fp16 [B,H,N,d], k and v fp16 [B,Hkv,Nk,d], key_lengths
+    int32 [B] or None. With Hkv = H and Nk = N the draws are those of draw()."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+
+    def normal(shape, sigma):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        if sigma != 1.0:
+            x *= np.float32(sigma)
+        return x.astype(np.float16)
+
+    q = normal((B, H, N, d), sigma_qk)
+    k = normal((B, Hkv, Nk, d), sigma_qk)
+    v = normal((B, Hkv, Nk, d), sigma_v)
+    kl = None
+    if key_len_range is not None:
+        lo, hi = key_len_range
+        kl = rng.integers(lo, hi + 1, size=B, dtype=np.int64).astype(np.int32)
+    return q, k, v, kl
+
+
 def draw_workload(w: Workload):
+    if w.Hkv is not None or w.Nk is not None:
+        return draw_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d, w.seed, sigma_qk=w.sigma_qk,
+                       sigma_v=w.sigma_v, key_len_range=w.key_len_range)
     return draw(w.B, w.H, w.N, w.d, w.seed, sigma_qk=w.sigma_qk, sigma_v=w.sigma_v,
                 key_len_range=w.key_len_range)
 
@@ -96,6 +144,28 @@ def attention_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
     """Contract FLOP count: 4*B*H*N^2*d (2d for QK^T and 2d for PV per pair), halved when causal."""
     f = 4.0 * B * H * N * N * d
     return f / 2 if causal else f
+
+
+def attention_flops_ex(B: int, H: int, N: int, Nk: int, d: int, causal: bool) -> float:
+    """Contract FLOP count of N queries over Nk keys: 4*B*H*N*Nk*d; under the causal mask
+    (query i sees keys j <= i + Nk - N) the same convention as attention_flops, i.e. the
+    allowed pairs counted as the area of the region, N*Nk - N^2/2 for N <= Nk."""
+    if not causal:
+        return 4.0 * B * H * N * Nk * d
+    if N <= Nk:
+        area = N * Nk - N * N / 2.0
+    else:
+        area = Nk * Nk / 2.0  # the first N - Nk rows see no key
+    return 4.0 * B * H * area * d
+
+
+def min_bytes_ex(B: int, H: int, Hkv: int, N: int, Nk: int, d: int, lse: bool = False) -> int:
+    """Minimum HBM traffic: Q read and O written ([B,H,N,d] fp16), K and V read once
+    ([B,Hkv,Nk,d] fp16), plus fp32 lse."""
+    b = 2 * B * H * N * d * 2 + 2 * B * Hkv * Nk * d * 2
+    if lse:
+        b += 4 * B * H * N
+    return b
 
 
 def min_bytes(B: int, H: int, N: int, d: int, lse: bool = False) -> int:

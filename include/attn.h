@@ -121,6 +121,32 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
                              attn_stream_t stream);
 
 /*
+ * Cross-attention and grouped-query attention (the "natural extensions" named in the
+ * "cuda-reranker" README): the forward of attn_fwd_path with separate query and key/value
+ * shapes.
+ *   q, o         fp16 [B, H, N_q, d]; lse (optional) fp32 [B, H, N_q]
+ *   k, v         fp16 [B, H_kv, N_k, d]; H must be a multiple of H_kv. Query head h reads
+ *                key/value head h / (H / H_kv) (groups of consecutive query heads share one
+ *                K, V; H_kv = H is multi-head attention, H_kv = 1 multi-query attention)
+ *   key_lengths  device int32 [B] or NULL: keys j >= key_lengths[b] (clamped to [0, N_k]) are
+ *                excluded
+ *   causal       query i sees keys j <= i + N_k - N_q: the diagonal is aligned at the last rows,
+ *                so the last query sees every key (a query block appended to a sequence of
+ *                N_k - N_q earlier tokens). The pages fix no alignment for N_q != N_k; this is
+ *                the reading taken. Rows with no allowed key get O = 0 and lse = -inf.
+ *   path         ATTN_PATH_AUTO (the short-sequence kernel for self-attention shapes where
+ *                attn_auto_path selects it, the tcgen05 kernel otherwise), ATTN_PATH_TCGEN05 or
+ *                ATTN_PATH_WARP_MMA; ATTN_PATH_SHORT takes self-attention shapes only
+ *                (H_kv = H, N_q = N_k), else ATTN_ERR_UNSUPPORTED.
+ * B, H, H_kv, N_q, N_k >= 1 (else ATTN_ERR_INVALID_ARG, as is H not a multiple of H_kv); the
+ * element count of every tensor must fit int64 and B*H int32. The other arguments, layouts
+ * and errors are those of attn_fwd_lse. With H_kv = H and N_q = N_k it is attn_fwd_path.
+ */
+attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int H, int H_kv, int N_q, int N_k, int d, float sm_scale, int causal,
+                          const int32_t *key_lengths, int path, attn_stream_t stream);
+
+/*
  * Split-KV forward: the same result as attn_fwd_lse (lse may be NULL), computed with the keys
  * of every (batch*head, pair of 128-row query tiles) divided into n_splits contiguous ranges of
  * 128-key tiles that run as separate work units (more parallel work when B*H*ceil(N/256) is
@@ -149,9 +175,24 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 
 /* The split count attn_fwd_splitkv uses for n_splits <= 0: enough (Q tile pair, key range)
  * units that the largest is no longer than an SM's average share on the current device (one
- * unit per SM without a causal mask, two with it, where the last pair has twice the average
- * work), at most one range per two 128-key tiles and at most 16. -1 for invalid sizes. */
+ * unit per SM without a causal mask; with it the largest pair's K/V tile count over the mean,
+ * about two), at most one range per two 128-key tiles and at most 16. -1 for invalid sizes. */
 int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal);
+
+/* Split-KV forward of cross-attention and grouped-query attention: the result of attn_fwd_ex
+ * (shapes, head groups and causal alignment as there), computed as attn_fwd_splitkv computes it.
+ * The workspace is sized by attn_splitkv_workspace_bytes(B, H, N_q, d, n_splits) (query rows);
+ * n_splits <= 0 takes attn_splitkv_auto_splits_ex(B, H, N_q, N_k, d, causal). With H_kv = H and
+ * N_q = N_k it is attn_fwd_splitkv. */
+attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int B, int H, int H_kv, int N_q, int N_k, int d, float sm_scale,
+                                  int causal, const int32_t *key_lengths, int n_splits,
+                                  void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* attn_splitkv_auto_splits for N_q query rows over N_k keys: under the causal mask the largest
+ * pair's work over the mean is taken from the pairs' 128-key tile counts with the diagonal of
+ * attn_fwd_ex. -1 for invalid sizes. */
+int attn_splitkv_auto_splits_ex(int B, int H, int N_q, int N_k, int d, int causal);
 
 /*
  * Split-KV forward that allocates nothing (the pages have no counterpart: this is a service of

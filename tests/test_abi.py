@@ -134,3 +134,38 @@ def test_noalloc_scratch_limit(lib):
     assert st == _lib.ATTN_ERR_SCRATCH_LIMIT
     assert lib.attn_fwd_splitkv_noalloc(A, A, A, A, None, 1, 1, 256, 64, 0.125, 0, None, 17,
                                         None) == _lib.ATTN_ERR_INVALID_ARG
+
+
+def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=64, scale=0.125,
+            causal=0, kl=None, path=0):
+    return lib.attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, kl, path, None)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(Hkv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=3), _lib.ATTN_ERR_INVALID_ARG),        # H not a multiple of H_kv
+    (dict(Hkv=8), _lib.ATTN_ERR_INVALID_ARG),        # more key/value heads than query heads
+    (dict(Nk=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(Nq=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(k=None), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(path=_lib.PATH_SHORT, d=32), _lib.ATTN_ERR_UNSUPPORTED),            # cross shape
+    (dict(path=_lib.PATH_SHORT, d=32, Nk=8), _lib.ATTN_ERR_UNSUPPORTED),      # grouped heads
+    (dict(v=A + 8), _lib.ATTN_ERR_MISALIGNED),
+    (dict(B=1 << 17, H=1 << 10, Hkv=1 << 10, Nq=8, Nk=1 << 30, d=128), _lib.ATTN_ERR_INVALID_ARG),
+])
+def test_fwd_ex_validation(lib, kw, expected):
+    assert call_ex(lib, **kw) == expected
+
+
+def test_splitkv_ex_validation(lib):
+    need = lib.attn_splitkv_workspace_bytes(1, 4, 8, 64, 2)
+    args = (A, A, A, A, None, 1, 4, 2, 8, 32, 64, 0.125, 0, None)
+    assert lib.attn_fwd_splitkv_ex(*args, 2, None, need, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_splitkv_ex(*args, 2, A, need - 1, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_splitkv_ex(*args, 17, A, 1 << 30, None) == _lib.ATTN_ERR_INVALID_ARG
+    bad = (A, A, A, A, None, 1, 4, 3, 8, 32, 64, 0.125, 0, None)
+    assert lib.attn_fwd_splitkv_ex(*bad, 2, A, 1 << 30, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 0, 64, 0) == -1
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 32, 48, 0) == -1
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 32, 64, 2) == -1
