@@ -8,8 +8,8 @@ forward over the whole batch with inputs resident in HBM. The same line carries:
   short_n      the reranking workload (B=50, H=12, N=256, d=32, key padding) in GB/s of
                minimum traffic, inputs rotated over buffer sets larger than L2
   split_kv     one long causal head, the tiled kernel alone and with split-KV
-  gqa          grouped-query prefill (32 query heads over 8 key/value heads) and a block of
-               1024 queries over 16384 cached keys, in TFLOP/s
+  variants     grouped-query prefill (32 query heads over 8 key/value heads), a block of
+               1024 queries over 16384 cached keys, and the prefill shape in bf16, in TFLOP/s
   roofline     the dominant kernel's achieved FLOP/s against the measured peak
   cpu_baseline the fp64 oracle timed on the host cores on a bounded sample (rank 0, N=1)
   clocks       SM clocks and throttle reasons sampled during the timed region
@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short-n", action="store_true")
     ap.add_argument("--no-split-kv", action="store_true")
-    ap.add_argument("--no-gqa", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
 
@@ -159,7 +159,8 @@ def oracle_sample(w, q, k, v, kl, heads):
     import oracle
     rows = np.concatenate([np.arange(h * w.N, (h + 1) * w.N) for h in heads]).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal, key_lengths=kl, rows=rows)
+    oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal, key_lengths=kl, rows=rows,
+                dtype=w.dtype)
     dt = time.perf_counter() - t0
     flops = synth.attention_flops_ex(1, len(heads), w.N, w.N_k, w.d, w.causal)
     return flops, dt, oracle.default_threads()
@@ -288,7 +289,7 @@ def main():
     steps, warmup = max(1, args.steps), max(3, args.warmup)
 
     q, k, v, kl = synth.draw_workload(w)
-    qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
     kld = torch.from_numpy(kl).cuda() if kl is not None else None
     od = torch.empty_like(qd)
     flops = synth.attention_flops_ex(w.B, w.H, w.N, w.N_k, w.d, w.causal)
@@ -333,9 +334,9 @@ def main():
 
     # End to end through the public API with host tensors.
     e2e_steps = max(1, min(args.e2e_steps, steps))
-    tq, tk, tv = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+    tq, tk, tv = (to_host(torch, x, w.dtype).pin_memory() for x in (q, k, v))
     tkl = torch.from_numpy(kl) if kl is not None else None
-    o_host = torch.empty(q.shape, dtype=torch.float16, pin_memory=True)
+    o_host = torch.empty(q.shape, dtype=tq.dtype, pin_memory=True)
     for _ in range(2):
         api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
                 path=args.path)
@@ -366,7 +367,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(workload_config(w), path=args.path, kernel=kernel_name),
         "e2e": {"value": weak_scaling_value(world, flops, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -379,8 +380,8 @@ def main():
         line["short_n"] = short_n(torch, api, peaks, peak_src)
     if not args.no_split_kv:
         line["split_kv"] = split_kv(torch, api, peaks, peak_src)
-    if not args.no_gqa:
-        line["gqa"] = gqa(torch, api, peaks, peak_src)
+    if not args.no_variants:
+        line["variants"] = variants(torch, api, peaks, peak_src)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # Bounded sample of the same workload: the first heads (flat batch*head order), all
@@ -499,17 +500,30 @@ def split_kv(torch, api, peaks, peak_src):
             "l2": "flushed (512 MiB write) before every timed launch; the split launch includes the merge kernel"}
 
 
-def gqa(torch, api, peaks, peak_src):
-    """Grouped-query and cross-attention shapes on the tiled kernel, TFLOP/s of the contract
-    count (allowed query/key pairs as the area under the causal diagonal); L2 flushed before
-    every timed launch."""
+def to_host(torch, x, dtype):
+    """numpy -> CPU tensor (uint16 bit patterns become torch.bfloat16 for bf16)."""
+    import numpy as np
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(x)
+
+
+def to_device(torch, x, dtype):
+    """numpy -> CUDA tensor (uint16 bit patterns become torch.bfloat16 for bf16)."""
+    return to_host(torch, x, dtype).cuda()
+
+
+def variants(torch, api, peaks, peak_src):
+    """Grouped-query and cross-attention shapes and bf16 inputs on the tiled kernel, TFLOP/s of
+    the contract count (allowed query/key pairs as the area under the causal diagonal); L2
+    flushed before every timed launch."""
     flush = l2_flush_buffer(torch)
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     out = {}
-    for name in ("gqa_prefill", "chunk_prefill"):
+    for name in ("gqa_prefill", "chunk_prefill", "prefill_bf16"):
         w = synth.WORKLOADS[name]
         q, k, v, _ = synth.draw_workload(w)
-        qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+        qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
         od = torch.empty_like(qd)
         flops = synth.attention_flops_ex(w.B, w.H, w.N, w.N_k, w.d, w.causal)
 
@@ -520,7 +534,7 @@ def gqa(torch, api, peaks, peak_src):
         ms = statistics.median(time_launches(torch, fn, 30, flush))
         tf = flops / (ms * 1e-3) / 1e12
         out[name] = {"workload": w.describe(), "value": tf, "unit": "TFLOP/s", "launch_ms": ms,
-                     "kernel": "tcgen05",
+                     "kernel": "tcgen05", "dtype": w.dtype,
                      "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
                                   "unit": "TFLOP/s", "frac": tf / peak,
                                   "peak_source": f"{peak_src} bf16 dense burst"}}

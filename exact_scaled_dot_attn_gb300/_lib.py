@@ -15,6 +15,9 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
 
+DTYPE_F16 = 0
+DTYPE_BF16 = 1
+
 PATH_AUTO = 0
 PATH_WARP_MMA = 1
 PATH_TCGEN05 = 2
@@ -46,9 +49,9 @@ SIGNATURES = {
     "attn_splitkv_auto_splits": (_i, [_i, _i, _i, _i, _i]),
     "attn_fwd_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
-    "attn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
-    "attn_fwd_splitkv_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp,
-                                 ctypes.c_size_t, _vp]),
+    "attn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_fwd_splitkv_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i,
+                                 _vp, ctypes.c_size_t, _vp]),
     "attn_splitkv_auto_splits_ex": (_i, [_i, _i, _i, _i, _i, _i]),
 }
 

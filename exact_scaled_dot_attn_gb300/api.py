@@ -31,9 +31,10 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
         sm_scale: float | None = None, key_lengths: torch.Tensor | None = None,
         return_lse: bool = False, out: torch.Tensor | None = None,
         lse_out: torch.Tensor | None = None, path: str = "auto"):
-    """O = softmax(sm_scale * Q K^T + mask) V for fp16 tensors: q [B, H, N, d] and k, v of the
-    same shape (self-attention) or [B, H_kv, N_k, d] (cross-attention and grouped-query
-    attention: H a multiple of H_kv, query head h reads key/value head h // (H // H_kv)).
+    """O = softmax(sm_scale * Q K^T + mask) V for fp16 or bf16 tensors (q, k, v and out of one
+    dtype; bf16 runs on the tcgen05 kernel): q [B, H, N, d] and k, v of the same shape
+    (self-attention) or [B, H_kv, N_k, d] (cross-attention and grouped-query attention: H a
+    multiple of H_kv, query head h reads key/value head h // (H // H_kv)).
 
     causal: key j allowed for query i only when j <= i + N_k - N (j <= i for self-attention).
     key_lengths: int32 [B]; keys j >= key_lengths[b] are excluded.
@@ -49,14 +50,15 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
                          return_lse=return_lse, out=out, lse_out=lse_out, path=path)
     B, H, N, d, Hkv, Nk = _shapes(q, k)
     dev = q.device
-    _check_device_tensor("q", q, (B, H, N, d), torch.float16, dev)
+    dt = _dtype_code(q)
+    _check_device_tensor("q", q, (B, H, N, d), q.dtype, dev)
     for name, t in (("k", k), ("v", v)):
-        _check_device_tensor(name, t, (B, Hkv, Nk, d), torch.float16, dev)
+        _check_device_tensor(name, t, (B, Hkv, Nk, d), q.dtype, dev)
     if dev.type != "cuda":
         raise ValueError("tensors must be CUDA tensors (or CPU tensors for the host path)")
     if out is None:
         out = torch.empty_like(q)
-    _check_device_tensor("out", out, (B, H, N, d), torch.float16, dev)
+    _check_device_tensor("out", out, (B, H, N, d), q.dtype, dev)
     lse = None
     if return_lse:
         lse = lse_out if lse_out is not None else torch.empty((B, H, N), device=dev,
@@ -72,7 +74,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
     lse_ptr = lse.data_ptr() if lse is not None else None
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-        if (Hkv, Nk) == (H, N):
+        if (Hkv, Nk) == (H, N) and dt == _lib.DTYPE_F16:
             what = "attn_fwd_path"
             st = _lib.lib().attn_fwd_path(
                 q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, N, d,
@@ -81,10 +83,18 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
             what = "attn_fwd_ex"
             st = _lib.lib().attn_fwd_ex(
                 q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, Hkv, N, Nk,
-                d, float(sm_scale), int(bool(causal)), kl_ptr, _lib.PATHS[path], stream)
+                d, dt, float(sm_scale), int(bool(causal)), kl_ptr, _lib.PATHS[path], stream)
     if st != _lib.ATTN_OK:
         raise _lib.AttnError(st, what)
     return (out, lse) if return_lse else out
+
+
+def _dtype_code(q):
+    if q.dtype == torch.float16:
+        return _lib.DTYPE_F16
+    if q.dtype == torch.bfloat16:
+        return _lib.DTYPE_BF16
+    raise TypeError(f"q must be torch.float16 or torch.bfloat16, got {q.dtype}")
 
 
 def _shapes(q, k):
@@ -112,12 +122,13 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("fwd_splitkv takes CUDA tensors")
-    _check_device_tensor("q", q, (B, H, N, d), torch.float16, dev)
+    dt = _dtype_code(q)
+    _check_device_tensor("q", q, (B, H, N, d), q.dtype, dev)
     for name, t in (("k", k), ("v", v)):
-        _check_device_tensor(name, t, (B, Hkv, Nk, d), torch.float16, dev)
+        _check_device_tensor(name, t, (B, Hkv, Nk, d), q.dtype, dev)
     if out is None:
         out = torch.empty_like(q)
-    _check_device_tensor("out", out, (B, H, N, d), torch.float16, dev)
+    _check_device_tensor("out", out, (B, H, N, d), q.dtype, dev)
     lse = None
     if return_lse:
         lse = lse_out if lse_out is not None else torch.empty((B, H, N), device=dev,
@@ -142,7 +153,7 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
         lse_ptr = lse.data_ptr() if lse is not None else None
         kl_ptr = key_lengths.data_ptr() if key_lengths is not None else None
         ws_bytes = workspace.numel() * workspace.element_size()
-        if (Hkv, Nk) == (H, N):
+        if (Hkv, Nk) == (H, N) and dt == _lib.DTYPE_F16:
             what = "attn_fwd_splitkv"
             st = L.attn_fwd_splitkv(
                 q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, N, d,
@@ -152,7 +163,7 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
             what = "attn_fwd_splitkv_ex"
             st = L.attn_fwd_splitkv_ex(
                 q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, Hkv, N,
-                Nk, d, float(sm_scale), int(bool(causal)), kl_ptr, int(n_splits),
+                Nk, d, dt, float(sm_scale), int(bool(causal)), kl_ptr, int(n_splits),
                 workspace.data_ptr(), ws_bytes, stream)
     if st != _lib.ATTN_OK:
         raise _lib.AttnError(st, what)
@@ -174,7 +185,7 @@ def _fwd_host(q, k, v, *, causal, sm_scale, key_lengths, return_lse, out, lse_ou
               return_lse=return_lse, path=path)
     o_dev, lse_dev = res if return_lse else (res, None)
     if out is None:
-        out = torch.empty(q.shape, dtype=torch.float16, pin_memory=True)
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     out.copy_(o_dev, non_blocking=True)
     if return_lse:
         if lse_out is None:

@@ -43,6 +43,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Sizes of one call: H query heads of N_q rows, H_kv key/value heads of N_k keys.
 struct Shape {
     int B, H, Hkv, Nq, Nk, d;
+    int dtype; // attn_dtype_t
     bool self() const { return Hkv == H && Nq == Nk; }
 };
 
@@ -58,6 +59,8 @@ attn_status_t validate(const void *q, const void *k, const void *v, const void *
     if (!std::isfinite(sm_scale))
         return ATTN_ERR_INVALID_ARG;
     if (sh.d != 32 && sh.d != 64 && sh.d != 128)
+        return ATTN_ERR_UNSUPPORTED;
+    if (sh.dtype != ATTN_DTYPE_F16 && sh.dtype != ATTN_DTYPE_BF16)
         return ATTN_ERR_UNSUPPORTED;
     const int64_t bh = static_cast<int64_t>(sh.B) * sh.H;
     if (bh > INT32_MAX)
@@ -89,6 +92,7 @@ attn::FwdParams make_params(const void *q, const void *k, const void *v, void *o
     p.d = sh.d;
     p.Hkv = sh.Hkv;
     p.Nk = sh.Nk;
+    p.dtype = sh.dtype == ATTN_DTYPE_BF16 ? attn::kDtypeBF16 : attn::kDtypeF16;
     p.sm_scale = sm_scale;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.causal = causal;
@@ -97,7 +101,7 @@ attn::FwdParams make_params(const void *q, const void *k, const void *v, void *o
     return p;
 }
 
-Shape self_shape(int B, int H, int N, int d) { return Shape{B, H, H, N, N, d}; }
+Shape self_shape(int B, int H, int N, int d) { return Shape{B, H, H, N, N, d, ATTN_DTYPE_F16}; }
 
 // One forward pass on the chosen kernel (the automatic choice when path is ATTN_PATH_AUTO).
 attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh,
@@ -143,11 +147,14 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
         path != ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
-    // The short-sequence kernel serves self-attention only.
+    // The short-sequence kernel serves fp16 self-attention only; bf16 runs on the tiled
+    // tcgen05 kernel only.
     if (path == ATTN_PATH_SHORT && (!sh.self() || sh.Nq > 256 || sh.d > 64))
         return ATTN_ERR_UNSUPPORTED;
+    if (sh.dtype == ATTN_DTYPE_BF16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05)
+        return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_AUTO)
-        path = sh.self() ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;
+        path = (sh.self() && sh.dtype == ATTN_DTYPE_F16) ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;
 
     attn::FwdParams p = make_params(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (opts && opts->wait_limit_ns)
@@ -180,12 +187,12 @@ extern "C" attn_status_t attn_fwd_debug(const void *q, const void *k, const void
 }
 
 extern "C" attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
-                                     int B, int H, int H_kv, int N_q, int N_k, int d, float sm_scale,
-                                     int causal, const int32_t *key_lengths, int path,
+                                     int B, int H, int H_kv, int N_q, int N_k, int d, int dtype,
+                                     float sm_scale, int causal, const int32_t *key_lengths, int path,
                                      attn_stream_t stream)
 {
-    return run_fwd(q, k, v, o, lse, Shape{B, H, H_kv, N_q, N_k, d}, sm_scale, causal, key_lengths, path,
-                   nullptr, stream);
+    return run_fwd(q, k, v, o, lse, Shape{B, H, H_kv, N_q, N_k, d, dtype}, sm_scale, causal, key_lengths,
+                   path, nullptr, stream);
 }
 
 extern "C" attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o,
@@ -290,11 +297,11 @@ extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal)
 
 extern "C" attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, void *o,
                                              float *lse, int B, int H, int H_kv, int N_q, int N_k, int d,
-                                             float sm_scale, int causal, const int32_t *key_lengths,
-                                             int n_splits, void *workspace, size_t workspace_bytes,
-                                             attn_stream_t stream)
+                                             int dtype, float sm_scale, int causal,
+                                             const int32_t *key_lengths, int n_splits, void *workspace,
+                                             size_t workspace_bytes, attn_stream_t stream)
 {
-    const Shape sh{B, H, H_kv, N_q, N_k, d};
+    const Shape sh{B, H, H_kv, N_q, N_k, d, dtype};
     attn_status_t st = validate(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
         return st;
@@ -327,8 +334,8 @@ extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const vo
                                           const int32_t *key_lengths, int n_splits, void *workspace,
                                           size_t workspace_bytes, attn_stream_t stream)
 {
-    return attn_fwd_splitkv_ex(q, k, v, o, lse, B, H, H, N, N, d, sm_scale, causal, key_lengths, n_splits,
-                               workspace, workspace_bytes, stream);
+    return attn_fwd_splitkv_ex(q, k, v, o, lse, B, H, H, N, N, d, ATTN_DTYPE_F16, sm_scale, causal,
+                               key_lengths, n_splits, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- split-KV without allocation

@@ -1,17 +1,23 @@
 // Internal interface between the C-ABI front end (attn_api.cu) and the kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace attn {
 
+// Element type of Q, K, V and O (16-bit storage; __half pointers below hold either).
+constexpr int kDtypeF16 = 0;
+constexpr int kDtypeBF16 = 1; // tcgen05 kernels only
+
 struct FwdParams {
     const __half *q;
     const __half *k;
     const __half *v;
     __half *o;
+    int dtype;                  // kDtypeF16 or kDtypeBF16
     float *lse;                 // may be null
     const int32_t *key_lengths; // may be null
     int B, H, N, d; // N: query rows per head

@@ -138,8 +138,6 @@ template <int D> struct Cfg {
     static constexpr int kOffKV = kQStages * 2 * kTileBytes;
     static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffBar + 1024 + 1024; // barriers + alignment slack
-    static constexpr uint32_t kIdescS = idesc_f16_f32(kBM, kBN, 0, 0);
-    static constexpr uint32_t kIdescPV = idesc_f16_f32(kBM, D, 0, 1);
 };
 
 struct TcArgs {
@@ -346,6 +344,7 @@ __device__ __forceinline__ float row_max_full(const uint32_t (&sv)[kBN], float s
 
 // p_e = 2^(S_e * scale - m) over a fully allowed row, rounded to fp16 pairs and stored to
 // TMEM at tP in two halves of 32 columns; returns sum_e p_e in fp32 (f32x2 arithmetic).
+template <bool BF16>
 __device__ __forceinline__ float exp_pack_full(const uint32_t (&sv)[kBN], float scale, float neg_m,
                                                uint32_t tP)
 {
@@ -365,7 +364,7 @@ __device__ __forceinline__ float exp_pack_full(const uint32_t (&sv)[kBN], float 
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-            pk[i >> 1] = pack_f16x2(p0, p1);
+            pk[i >> 1] = pack2<BF16>(p0, p1);
         }
         tmem_st32(tP + half * 32, pk);
     }
@@ -402,6 +401,7 @@ __device__ __forceinline__ float row_max(const uint32_t (&sv)[kBN], float scale,
 // pairs and stored to TMEM at tP (two halves of 32 columns, so only half of the packed
 // row is held in registers at a time); returns sum_e p_e in fp32. Pairs of lanes use
 // f32x2 arithmetic; fully masked chunks store zeros without evaluating any exponential.
+template <bool BF16>
 __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale, float neg_m, int lim,
                                           uint32_t tP)
 {
@@ -425,7 +425,7 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
                     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                     acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-                    pk[cc * 16 + (i >> 1)] = pack_f16x2(p0, p1);
+                    pk[cc * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
                 }
             } else if (lim > c * kChunkCols) {
 #pragma unroll
@@ -436,7 +436,7 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
                     const float p0 = e < lim ? ex2_approx(x0) : 0.f;
                     const float p1 = e + 1 < lim ? ex2_approx(x1) : 0.f;
                     acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-                    pk[cc * 16 + (i >> 1)] = pack_f16x2(p0, p1);
+                    pk[cc * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
                 }
             } else {
 #pragma unroll
@@ -452,7 +452,8 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
     return (a0 + a1) + (b0 + b1);
 }
 
-template <int D, bool SPLIT>
+// BF16: Q, K, V, O (and P) are bf16 instead of fp16.
+template <int D, bool SPLIT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tcgen05_kernel(const TcArgs args, const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
@@ -461,6 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using C = Cfg<D>;
     using BB = Bars<D>;
+    // S = Q K^T: both K-major; O += P V: P from TMEM, V MN-major. A and B share one type.
+    constexpr uint32_t kIdescS = idesc_f16_f32(kBM, kBN, 0, 0, BF16);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kBM, D, 0, 1, BF16);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -623,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < D / 16; ++kk) {
                 constexpr int kBox16 = C::kBoxBytes >> 4;
                 const uint32_t off = (kk / kStepsPerBox) * kBox16 + (kk % kStepsPerBox) * 2;
-                mma_ss(d_tmem, desc(qlo + off), desc(klo + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                mma_ss(d_tmem, desc(qlo + off), desc(klo + off), kIdescS, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar(BB::kSFull + t));
         };
@@ -637,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
                 mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((16 * C::kRowBytes) >> 4)),
-                       C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
             mma_commit(bar(BB::kOReady + t * 2 + b));
         };
         UnitStream us;
@@ -829,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t h[kChunk / 2];
 #pragma unroll
                 for (int e = 0; e < kChunk; e += 2)
-                    h[e >> 1] = pack_f16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+                    h[e >> 1] = pack2<BF16>(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
                 if (pe.row < p.N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
 #pragma unroll
@@ -903,8 +907,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
 
                 // P = exp2(S * scale - m_ref) as fp16, written over the first 64 columns of S
-                const float rs = need_mask ? exp_pack(sv, scale, neg_m, lim, tS)
-                                           : exp_pack_full(sv, scale, neg_m, tS);
+                const float rs = need_mask ? exp_pack<BF16>(sv, scale, neg_m, lim, tS)
+                                           : exp_pack_full<BF16>(sv, scale, neg_m, tS);
                 // O holds the PV products of earlier tiles; rescale it (after the last of
                 // them is done) before this tile's P is released to the MMA warp. The warp
                 // does it together when any of its rows needs it (tcgen05.ld/st are
@@ -977,18 +981,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // [heads, rows, D] fp16 viewed as a 3-D tensor (D innermost): Q is [B*H, N, D], K and V
 // [B*Hkv, Nk, D]; boxes of 128 rows x 64 columns with a 128-byte swizzle (x 32 columns with
 // a 64-byte swizzle for D = 32); rows past the end read as zero.
-bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D)
+bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, bool bf16)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
         return false;
+    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(D < 64 ? D : 64), static_cast<cuuint32_t>(kBM), 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+    return enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE,
                D < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1079,7 +1084,7 @@ std::shared_ptr<SchedTable> schedule_for(int BH, int N, int Nk, int causal, int 
     return t;
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool BF16>
 cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpart, cudaStream_t stream,
                      unsigned int *status)
 {
@@ -1089,8 +1094,8 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
         return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     CUtensorMap mq, mk, mv;
-    if (!encode_map(&mq, p.q, BH, p.N, D) || !encode_map(&mk, p.k, BHkv, p.Nk, D) ||
-        !encode_map(&mv, p.v, BHkv, p.Nk, D))
+    if (!encode_map(&mq, p.q, BH, p.N, D, BF16) || !encode_map(&mk, p.k, BHkv, p.Nk, D, BF16) ||
+        !encode_map(&mv, p.v, BHkv, p.Nk, D, BF16))
         return cudaErrorInvalidValue;
     TcArgs a;
     a.p = p;
@@ -1108,7 +1113,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
     cudaError_t err = device_sm_count(&sms);
     if (err != cudaSuccess)
         return err;
-    auto kernel = attn_fwd_tcgen05_kernel<D, SPLIT>;
+    auto kernel = attn_fwd_tcgen05_kernel<D, SPLIT, BF16>;
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess)
         return err;
@@ -1131,7 +1136,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
 // logsumexp of range s and O_s its normalised output, lse = log sum_s exp(lse_s) and
 // O = sum_s exp(lse_s - lse) O_s. Ranges without an allowed key (lse_s = -inf) weigh 0; a
 // row with none at all gets O = 0 and lse = -inf.
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
     attn_splitkv_merge_kernel(const float *__restrict__ opart, const float *__restrict__ lpart,
                               __half *__restrict__ o, float *__restrict__ lse, long long rows, int S)
@@ -1165,15 +1170,20 @@ __global__ void __launch_bounds__(256)
             acc[c] += w * src[c];
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    // O (16-bit elements: bf16 when BF16, fp16 otherwise), rounded to nearest even
     __half *dst = o + row * D + lane * kPer;
 #pragma unroll
-    for (int c = 0; c < kPer; ++c)
-        dst[c] = __float2half_rn(acc[c] * inv);
+    for (int c = 0; c < kPer; ++c) {
+        if constexpr (BF16)
+            reinterpret_cast<__nv_bfloat16 *>(dst)[c] = __float2bfloat16_rn(acc[c] * inv);
+        else
+            dst[c] = __float2half_rn(acc[c] * inv);
+    }
     if (lse && lane == 0)
         lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
-template <int D>
+template <int D, bool BF16>
 cudaError_t launch_merge(const FwdParams &p, int n_splits, const float *opart, const float *lpart,
                          cudaStream_t stream)
 {
@@ -1181,19 +1191,53 @@ cudaError_t launch_merge(const FwdParams &p, int n_splits, const float *opart, c
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    attn_splitkv_merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    attn_splitkv_merge_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         opart, lpart, p.o, p.lse, rows, n_splits);
     return cudaGetLastError();
 }
 
 } // namespace
 
-cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
+namespace {
+
+template <bool BF16>
+cudaError_t launch_tcgen05_t(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
     switch (p.d) {
-    case 32: return launch_d<32, false>(p, 1, nullptr, nullptr, stream, status);
-    case 64: return launch_d<64, false>(p, 1, nullptr, nullptr, stream, status);
-    case 128: return launch_d<128, false>(p, 1, nullptr, nullptr, stream, status);
+    case 32: return launch_d<32, false, BF16>(p, 1, nullptr, nullptr, stream, status);
+    case 64: return launch_d<64, false, BF16>(p, 1, nullptr, nullptr, stream, status);
+    case 128: return launch_d<128, false, BF16>(p, 1, nullptr, nullptr, stream, status);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_splitkv_t(const FwdParams &p, int n_splits, float *opart, float *lpart,
+                             cudaStream_t stream, unsigned int *status)
+{
+    cudaError_t err;
+    switch (p.d) {
+    case 32: err = launch_d<32, true, BF16>(p, n_splits, opart, lpart, stream, status); break;
+    case 64: err = launch_d<64, true, BF16>(p, n_splits, opart, lpart, stream, status); break;
+    case 128: err = launch_d<128, true, BF16>(p, n_splits, opart, lpart, stream, status); break;
+    default: return cudaErrorInvalidValue;
+    }
+    if (err != cudaSuccess)
+        return err;
+    switch (p.d) {
+    case 32: return launch_merge<32, BF16>(p, n_splits, opart, lpart, stream);
+    case 64: return launch_merge<64, BF16>(p, n_splits, opart, lpart, stream);
+    default: return launch_merge<128, BF16>(p, n_splits, opart, lpart, stream);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
+{
+    switch (p.dtype) {
+    case kDtypeF16: return launch_tcgen05_t<false>(p, stream, status);
+    case kDtypeBF16: return launch_tcgen05_t<true>(p, stream, status);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1201,19 +1245,10 @@ cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int
 cudaError_t launch_tcgen05_splitkv(const FwdParams &p, int n_splits, float *opart, float *lpart,
                                    cudaStream_t stream, unsigned int *status)
 {
-    cudaError_t err;
-    switch (p.d) {
-    case 32: err = launch_d<32, true>(p, n_splits, opart, lpart, stream, status); break;
-    case 64: err = launch_d<64, true>(p, n_splits, opart, lpart, stream, status); break;
-    case 128: err = launch_d<128, true>(p, n_splits, opart, lpart, stream, status); break;
+    switch (p.dtype) {
+    case kDtypeF16: return launch_splitkv_t<false>(p, n_splits, opart, lpart, stream, status);
+    case kDtypeBF16: return launch_splitkv_t<true>(p, n_splits, opart, lpart, stream, status);
     default: return cudaErrorInvalidValue;
-    }
-    if (err != cudaSuccess)
-        return err;
-    switch (p.d) {
-    case 32: return launch_merge<32>(p, n_splits, opart, lpart, stream);
-    case 64: return launch_merge<64>(p, n_splits, opart, lpart, stream);
-    default: return launch_merge<128>(p, n_splits, opart, lpart, stream);
     }
 }
 

@@ -167,12 +167,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with fp16 A and B and fp32 D.
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D and A, B both fp16 (bf16 = 0)
+// or both bf16 (bf16 = 1): one kind::f16 MMA never mixes the two.
 // a_mn / b_mn: 1 when the operand is MN-major (transposed) in shared memory.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn)
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn, int bf16 = 0)
 {
     return (1u << 4)                                   // D format: f32
-           | (0u << 7) | (0u << 10)                    // A, B format: f16
+           | (static_cast<uint32_t>(bf16 ? 1 : 0) << 7)  // A format: f16 (0) or bf16 (1)
+           | (static_cast<uint32_t>(bf16 ? 1 : 0) << 10) // B format: the same as A
            | (static_cast<uint32_t>(a_mn) << 15)       // A major
            | (static_cast<uint32_t>(b_mn) << 16)       // B major
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
@@ -334,6 +336,22 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     // cvt packs the first source operand into the upper half.
     asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two fp32 values rounded to nearest even and packed as 16-bit floats (bf16 or fp16).
+template <bool BF16> __device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (BF16)
+        return pack_bf16x2(lo, hi);
+    else
+        return pack_f16x2(lo, hi);
 }
 
 // Packed pairs of fp32 (Blackwell f32x2 arithmetic: two lanes per instruction).

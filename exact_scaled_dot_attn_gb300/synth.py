@@ -10,7 +10,8 @@ Recipe (one numpy PCG64 stream per workload, seeded with the workload's seed):
   (round-to-nearest-even), shape [B, H, N, d]; then, for padded workloads,
   key_lengths[b] ~ uniform integer in [lo, hi] (inclusive). Cross-attention and
   grouped-query workloads draw Q as [B, H, N, d] and K, V as [B, H_kv, N_k, d] in the
-  same order.
+  same order. bf16 workloads round the same float32 draws to bfloat16 (nearest even)
+  and hold them as uint16 bit patterns.
 
 The shapes are the workloads the method is measured on: a tiny exact check, a
 cross-encoder reranking batch (the "cuda-reranker" README's shape class: many
@@ -44,6 +45,7 @@ class Workload:
     ignore_padded_queries: bool = False
     Hkv: int | None = None  # key/value heads (None: H, multi-head attention)
     Nk: int | None = None   # keys per head (None: N, self-attention)
+    dtype: str = "f16"      # "f16" or "bf16" (uint16 bit patterns)
 
     @property
     def H_kv(self) -> int:
@@ -66,7 +68,8 @@ class Workload:
             kv += f" H_kv={self.H_kv}"
         if self.N_k != self.N:
             kv += f" N_k={self.N_k}"
-        return f"{self.name} B={self.B} H={self.H} N={self.N}{kv} d={self.d} {mask}"
+        dt = "" if self.dtype == "f16" else f" {self.dtype}"
+        return f"{self.name} B={self.B} H={self.H} N={self.N}{kv} d={self.d}{dt} {mask}"
 
 
 WORKLOADS = {
@@ -84,7 +87,16 @@ WORKLOADS = {
     # a block of 1024 new queries over a cached context of 16384 keys (cross-attention shape,
     # causal diagonal at the last rows), grouped-query heads
     "chunk_prefill": Workload("chunk_prefill", 2, 32, 1024, 128, True, seed=8, Hkv=8, Nk=16384),
+    # the prefill shape with bf16 inputs
+    "prefill_bf16": Workload("prefill_bf16", 4, 32, 4096, 128, True, seed=9, dtype="bf16"),
 }
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), rounded to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
 
 
 def draw(B: int, H: int, N: int, d: int, seed: int, *, sigma_qk: float = 1.0,
@@ -111,16 +123,19 @@ def draw(B: int, H: int, N: int, d: int, seed: int, *, sigma_qk: float = 1.0,
 
 def draw_ex(B: int, H: int, Hkv: int, N: int, Nk: int, d: int, seed: int, *,
             sigma_qk: float = 1.0, sigma_v: float = 1.0,
-            key_len_range: tuple[int, int] | None = None):
-    """Returns (q, k, v, key_lengths): q fp16 [B,H,N,d], k and v fp16 [B,Hkv,Nk,d], key_lengths
-    int32 [B] or None. With Hkv = H and Nk = N the draws are those of draw()."""
+            key_len_range: tuple[int, int] | None = None, dtype: str = "f16"):
+    """Returns (q, k, v, key_lengths): q [B,H,N,d], k and v [B,Hkv,Nk,d] (fp16, or uint16
+    bfloat16 bit patterns for dtype "bf16"), key_lengths int32 [B] or None. With Hkv = H,
+    Nk = N and fp16 the draws are those of draw()."""
+    if dtype not in ("f16", "bf16"):
+        raise ValueError("dtype must be 'f16' or 'bf16'")
     rng = np.random.Generator(np.random.PCG64(seed))
 
     def normal(shape, sigma):
         x = rng.standard_normal(shape, dtype=np.float32)
         if sigma != 1.0:
             x *= np.float32(sigma)
-        return x.astype(np.float16)
+        return x.astype(np.float16) if dtype == "f16" else to_bf16_bits(x)
 
     q = normal((B, H, N, d), sigma_qk)
     k = normal((B, Hkv, Nk, d), sigma_qk)
@@ -133,9 +148,9 @@ def draw_ex(B: int, H: int, Hkv: int, N: int, Nk: int, d: int, seed: int, *,
 
 
 def draw_workload(w: Workload):
-    if w.Hkv is not None or w.Nk is not None:
+    if w.Hkv is not None or w.Nk is not None or w.dtype != "f16":
         return draw_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d, w.seed, sigma_qk=w.sigma_qk,
-                       sigma_v=w.sigma_v, key_len_range=w.key_len_range)
+                       sigma_v=w.sigma_v, key_len_range=w.key_len_range, dtype=w.dtype)
     return draw(w.B, w.H, w.N, w.d, w.seed, sigma_qk=w.sigma_qk, sigma_v=w.sigma_v,
                 key_len_range=w.key_len_range)
 

@@ -64,6 +64,14 @@ typedef enum {
                                   attn_noalloc_scratch_bytes() */
 } attn_status_t;
 
+/* Element type of Q, K, V and O for attn_fwd_ex / attn_fwd_splitkv_ex (the other entry points
+ * take fp16). bf16 (8-bit exponent, 8-bit significand) runs on the tiled tcgen05 kernel only,
+ * with P rounded to bf16 as well: one tcgen05 MMA takes A and B of the same type. */
+typedef enum {
+    ATTN_DTYPE_F16 = 0,
+    ATTN_DTYPE_BF16 = 1
+} attn_dtype_t;
+
 /* Which kernel runs the forward. AUTO runs the short-sequence kernel for d = 32 with
  * N <= 256 and the tiled tcgen05 kernel everywhere else (the fastest at every measured
  * shape); the other kernels remain selectable explicitly. */
@@ -134,17 +142,19 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
  *                so the last query sees every key (a query block appended to a sequence of
  *                N_k - N_q earlier tokens). The pages fix no alignment for N_q != N_k; this is
  *                the reading taken. Rows with no allowed key get O = 0 and lse = -inf.
- *   path         ATTN_PATH_AUTO (the short-sequence kernel for self-attention shapes where
- *                attn_auto_path selects it, the tcgen05 kernel otherwise), ATTN_PATH_TCGEN05 or
- *                ATTN_PATH_WARP_MMA; ATTN_PATH_SHORT takes self-attention shapes only
- *                (H_kv = H, N_q = N_k), else ATTN_ERR_UNSUPPORTED.
+ *   dtype        attn_dtype_t of q, k, v and o (all four the same): ATTN_DTYPE_F16, or
+ *                ATTN_DTYPE_BF16 (tcgen05 kernel only); another value is ATTN_ERR_UNSUPPORTED
+ *   path         ATTN_PATH_AUTO (for fp16 self-attention shapes the kernel attn_auto_path
+ *                selects, the tcgen05 kernel otherwise), ATTN_PATH_TCGEN05 or
+ *                ATTN_PATH_WARP_MMA (fp16); ATTN_PATH_SHORT takes fp16 self-attention shapes
+ *                only (H_kv = H, N_q = N_k); any other combination is ATTN_ERR_UNSUPPORTED.
  * B, H, H_kv, N_q, N_k >= 1 (else ATTN_ERR_INVALID_ARG, as is H not a multiple of H_kv); the
  * element count of every tensor must fit int64 and B*H int32. The other arguments, layouts
- * and errors are those of attn_fwd_lse. With H_kv = H and N_q = N_k it is attn_fwd_path.
+ * and errors are those of attn_fwd_lse. With H_kv = H, N_q = N_k and fp16 it is attn_fwd_path.
  */
 attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                          int H, int H_kv, int N_q, int N_k, int d, float sm_scale, int causal,
-                          const int32_t *key_lengths, int path, attn_stream_t stream);
+                          int H, int H_kv, int N_q, int N_k, int d, int dtype, float sm_scale,
+                          int causal, const int32_t *key_lengths, int path, attn_stream_t stream);
 
 /*
  * Split-KV forward: the same result as attn_fwd_lse (lse may be NULL), computed with the keys
@@ -180,14 +190,16 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
 /* Split-KV forward of cross-attention and grouped-query attention: the result of attn_fwd_ex
- * (shapes, head groups and causal alignment as there), computed as attn_fwd_splitkv computes it.
+ * (shapes, head groups, causal alignment and dtype as there), computed as attn_fwd_splitkv
+ * computes it.
  * The workspace is sized by attn_splitkv_workspace_bytes(B, H, N_q, d, n_splits) (query rows);
  * n_splits <= 0 takes attn_splitkv_auto_splits_ex(B, H, N_q, N_k, d, causal). With H_kv = H and
- * N_q = N_k it is attn_fwd_splitkv. */
+ * N_q = N_k and fp16 it is attn_fwd_splitkv. */
 attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, void *o, float *lse,
-                                  int B, int H, int H_kv, int N_q, int N_k, int d, float sm_scale,
-                                  int causal, const int32_t *key_lengths, int n_splits,
-                                  void *workspace, size_t workspace_bytes, attn_stream_t stream);
+                                  int B, int H, int H_kv, int N_q, int N_k, int d, int dtype,
+                                  float sm_scale, int causal, const int32_t *key_lengths,
+                                  int n_splits, void *workspace, size_t workspace_bytes,
+                                  attn_stream_t stream);
 
 /* attn_splitkv_auto_splits for N_q query rows over N_k keys: under the causal mask the largest
  * pair's work over the mean is taken from the pairs' 128-key tile counts with the diagonal of

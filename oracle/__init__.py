@@ -43,6 +43,8 @@ class Oracle:
         lib = ctypes.CDLL(lib_path)
         lib.oracle_half_to_double.restype = ctypes.c_double
         lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_attn.restype = ctypes.c_int
         lib.oracle_attn.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -54,7 +56,7 @@ class Oracle:
         lib.oracle_attn_ex.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-            ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
         self._lib = lib
@@ -63,11 +65,17 @@ class Oracle:
         """Decode one binary16 bit pattern with the oracle's own decoder."""
         return self._lib.oracle_half_to_double(bits)
 
+    def bf16_to_double(self, bits: int) -> float:
+        """Decode one bfloat16 bit pattern with the oracle's own decoder."""
+        return self._lib.oracle_bf16_to_double(bits)
+
     def attn(self, q, k, v, *, sm_scale: float, causal: bool = False, key_lengths=None,
-             rows=None, threads: int | None = None):
+             rows=None, threads: int | None = None, dtype: str = "f16"):
         """Oracle forward.
 
-        q: numpy float16 array [B, H, N, d] (N query rows per head); k, v: [B, Hkv, Nk, d]
+        dtype "f16": q, k, v are numpy float16 arrays; "bf16": numpy uint16 (or int16) arrays
+        of bfloat16 bit patterns.
+        q: [B, H, N, d] (N query rows per head); k, v: [B, Hkv, Nk, d]
         with H a multiple of Hkv (query head h reads key/value head h // (H // Hkv)).
         Self-attention is k, v of q's shape. With causal and Nk != N, query i sees
         keys j <= i + Nk - N.
@@ -76,9 +84,17 @@ class Oracle:
         Returns (o, lse) as float64: o is [B,H,N,d] (or [len(rows), d]), lse is
         [B,H,N] (or [len(rows)]).
         """
-        q = np.ascontiguousarray(q, dtype=np.float16)
-        k = np.ascontiguousarray(k, dtype=np.float16)
-        v = np.ascontiguousarray(v, dtype=np.float16)
+        if dtype == "f16":
+            code = 0
+            q, k, v = (np.ascontiguousarray(x, dtype=np.float16) for x in (q, k, v))
+        elif dtype == "bf16":
+            code = 1
+            for x in (q, k, v):
+                if np.asarray(x).dtype not in (np.uint16, np.int16):
+                    raise TypeError("bf16 inputs are uint16/int16 arrays of bit patterns")
+            q, k, v = (np.ascontiguousarray(x).view(np.uint16) for x in (q, k, v))
+        else:
+            raise ValueError("dtype must be 'f16' or 'bf16'")
         if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape:
             raise ValueError("q must be [B,H,N,d] and k, v one [B,Hkv,Nk,d] shape")
         B, H, N, d = q.shape
@@ -101,7 +117,7 @@ class Oracle:
             o = np.empty((n_rows, d), np.float64)
             lse = np.empty((n_rows,), np.float64)
         rc = self._lib.oracle_attn_ex(
-            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Hkv, N, Nk, d, float(sm_scale),
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Hkv, N, Nk, d, code, float(sm_scale),
             int(bool(causal)), None if kl is None else kl.ctypes.data,
             None if rows_arr is None else rows_arr.ctypes.data, n_rows,
             o.ctypes.data, lse.ctypes.data, int(threads or default_threads()))

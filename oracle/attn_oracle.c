@@ -6,8 +6,8 @@
  * and its Python binding) never calls it, and this file includes nothing from
  * the product path.
  *
- * What it computes, for every batch b, query head h and query row i (inputs fp16,
- * d innermost; Q and O [B,H,Nq,d], K and V [B,Hkv,Nk,d]; query head h reads key/value
+ * What it computes, for every batch b, query head h and query row i (inputs fp16 or
+ * bf16, d innermost; Q and O [B,H,Nq,d], K and V [B,Hkv,Nk,d]; query head h reads key/value
  * head h / (H / Hkv), grouped-query attention, Hkv = H being multi-head attention;
  * self-attention is Nq = Nk = N):
  *
@@ -46,7 +46,8 @@
  *
  * The score row is held explicitly (one row of S at a time, never the N x N
  * matrix) and the softmax is the two-pass definition. Inputs are decoded from
- * IEEE-754 binary16 to double exactly, so input rounding is not an error source.
+ * IEEE-754 binary16 (or bfloat16) to double exactly, so input rounding is not an
+ * error source.
  * Work is split across POSIX threads over (batch*head, block of query rows).
  */
 #include <math.h>
@@ -73,13 +74,34 @@ double oracle_half_to_double(uint16_t h)
     return sign ? -mag : mag;
 }
 
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.
+ * exponent 0: subnormal, value = f * 2^-133; exponent 255: inf (f == 0) or NaN;
+ * otherwise value = (128 + f) * 2^(e - 134). Exact in double. */
+double oracle_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -133);
+    else if (e == 255)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(128 + f), e - 134);
+    return sign ? -mag : mag;
+}
+
 static double g_half_table[65536];
+static double g_bf16_table[65536];
 static pthread_once_t g_table_once = PTHREAD_ONCE_INIT;
 
 static void build_half_table(void)
 {
-    for (uint32_t h = 0; h < 65536u; ++h)
+    for (uint32_t h = 0; h < 65536u; ++h) {
         g_half_table[h] = oracle_half_to_double((uint16_t)h);
+        g_bf16_table[h] = oracle_bf16_to_double((uint16_t)h);
+    }
 }
 
 /* Key j is in query i's allowed set; off = Nk - Nq places the causal diagonal. */
@@ -134,6 +156,7 @@ typedef struct {
     const uint16_t *q, *k, *v;
     int64_t B, H, N, d; /* N: query rows per head */
     int64_t Hkv, Nk;    /* key/value heads per batch, keys per head */
+    const double *dec;  /* decode table of the input format (fp16 or bf16) */
     double sm_scale;
     int causal;
     const int32_t *key_lengths;
@@ -181,14 +204,14 @@ static void *worker(void *arg)
             if (kvh != decoded_head) {
                 const uint16_t *kh = J->k + kvh * Nk * d, *vh = J->v + kvh * Nk * d;
                 for (int64_t e = 0; e < Nk * d; ++e) {
-                    K[e] = g_half_table[kh[e]];
-                    V[e] = g_half_table[vh[e]];
+                    K[e] = J->dec[kh[e]];
+                    V[e] = J->dec[vh[e]];
                 }
                 decoded_head = kvh;
             }
             const uint16_t *qr = J->q + r * d;
             for (int64_t c = 0; c < d; ++c)
-                q[c] = g_half_table[qr[c]];
+                q[c] = J->dec[qr[c]];
             int64_t L = Nk;
             if (J->key_lengths) {
                 L = J->key_lengths[b];
@@ -208,20 +231,20 @@ static void *worker(void *arg)
 
 /*
  * Computes O (and lse) for the listed query rows, or for all B*H*Nq rows when
- * rows == NULL. q: fp16 bit patterns [B,H,Nq,d]; k, v: [B,Hkv,Nk,d], H a multiple
- * of Hkv. key_lengths: [B] or NULL. rows: flat row ids (b*H + h)*Nq + i in
+ * rows == NULL. q: 16-bit float bit patterns [B,H,Nq,d]; k, v: [B,Hkv,Nk,d], H a
+ * multiple of Hkv; dtype 0: IEEE binary16, 1: bfloat16. key_lengths: [B] or NULL. rows: flat row ids (b*H + h)*Nq + i in
  * ascending order, n_rows of them. o: [n_rows, d] doubles (or [B,H,Nq,d] when
  * rows == NULL); lse: [n_rows] or NULL. n_threads <= 0 uses one thread. Returns 0
  * on success, -1 on bad arguments, -2 when memory runs out.
  */
 int oracle_attn_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B, int64_t H,
-                   int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, double sm_scale, int causal,
-                   const int32_t *key_lengths, const int64_t *rows, int64_t n_rows, double *o,
-                   double *lse, int n_threads)
+                   int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int dtype, double sm_scale,
+                   int causal, const int32_t *key_lengths, const int64_t *rows, int64_t n_rows,
+                   double *o, double *lse, int n_threads)
 {
     const int64_t N = Nq;
     if (!q || !k || !v || !o || B < 0 || H < 0 || N < 0 || Nk < 0 || d <= 0 || Hkv < 1 ||
-        H % Hkv != 0)
+        H % Hkv != 0 || (dtype != 0 && dtype != 1))
         return -1;
     int64_t total = B * H * N;
     if (!rows)
@@ -257,6 +280,7 @@ int oracle_attn_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
     J.q = q; J.k = k; J.v = v;
     J.B = B; J.H = H; J.N = N; J.d = d;
     J.Hkv = Hkv; J.Nk = Nk;
+    J.dec = dtype == 1 ? g_bf16_table : g_half_table;
     J.sm_scale = sm_scale;
     J.causal = causal;
     J.key_lengths = key_lengths;
@@ -298,6 +322,6 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t
                 int64_t N, int64_t d, double sm_scale, int causal, const int32_t *key_lengths,
                 const int64_t *rows, int64_t n_rows, double *o, double *lse, int n_threads)
 {
-    return oracle_attn_ex(q, k, v, B, H, H > 0 ? H : 1, N, N, d, sm_scale, causal, key_lengths,
+    return oracle_attn_ex(q, k, v, B, H, H > 0 ? H : 1, N, N, d, 0, sm_scale, causal, key_lengths,
                           rows, n_rows, o, lse, n_threads);
 }

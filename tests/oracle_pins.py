@@ -8,6 +8,8 @@ that a plausible mistake anywhere in the oracle fails at least one pin.
 What pins what:
   worked examples printed on the pages (tests/golden/)   -> dot product, softmax values
   numpy's own binary16 -> float64 conversion             -> the fp16 decoder
+  numpy's float32 bit view (bfloat16 = upper half)        -> the bf16 decoder
+  values exact in both formats (fp16 vs bf16 result)      -> bf16 routing
   scipy.special.softmax / logsumexp on tiny inputs       -> scores, masks, softmax, PV, lse
   P1's two-block online-softmax merge                     -> normalisation and lse
   closed forms (uniform keys, one-hot selection, causal
@@ -388,6 +390,46 @@ def pin_cross_gqa_uniform_keys(orc):
                     assert abs(lse[b, h, i] - (s + math.log(n))) < 1e-12
 
 
+def pin_bf16_decoder(orc):
+    """bfloat16 is the upper half of an IEEE binary32: every bit pattern b decodes as numpy's
+    float32 with bits b << 16 (converted to float64)."""
+    bits = np.arange(65536, dtype=np.uint32)
+    ref = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([orc.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def pin_bf16_agrees_with_f16_on_common_values(orc):
+    """Inputs whose values are exact in both formats (multiples of 1/16 up to 4 in magnitude,
+    and powers of two from 2^-10 to 2^3) decode to the same doubles, so the bf16 and fp16
+    results are the same bits; a wrong decode table or format routing breaks this."""
+    rng = np.random.Generator(np.random.PCG64(231))
+    vals = np.concatenate([np.arange(-64, 65) / 16.0, 2.0 ** np.arange(-10, 4),
+                           -(2.0 ** np.arange(-10, 4))])
+    B, H, Hkv, Nq, Nk, d = 2, 4, 2, 9, 13, 8
+    q64, k64, v64 = (rng.choice(vals, size=sh) for sh in
+                     ((B, H, Nq, d), (B, Hkv, Nk, d), (B, Hkv, Nk, d)))
+
+    def as_bf16(x):
+        return (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+    for causal in (False, True):
+        kl = np.array([13, 5], np.int32)
+        o16, l16 = orc.attn(q64.astype(np.float16), k64.astype(np.float16), v64.astype(np.float16),
+                            sm_scale=0.3, causal=causal, key_lengths=kl)
+        ob, lb = orc.attn(as_bf16(q64), as_bf16(k64), as_bf16(v64), sm_scale=0.3, causal=causal,
+                          key_lengths=kl, dtype="bf16")
+        assert np.array_equal(o16, ob) and np.array_equal(l16, lb)
+    # values outside fp16's range are finite in bf16: 2^20 * 2^-20 products give score 1 per term
+    big = np.full((1, 1, 2, 1), 2.0 ** 20)
+    small = np.full((1, 1, 2, 1), 2.0 ** -20)
+    o, lse = orc.attn(as_bf16(big), as_bf16(small), as_bf16(np.array([1.0, 3.0]).reshape(1, 1, 2, 1)),
+                      sm_scale=1.0, dtype="bf16")
+    assert np.allclose(o, 2.0, atol=1e-12, rtol=0) and np.allclose(lse, 1.0 + math.log(2.0))
+
+
 ALL_PINS = [
     pin_half_decoder,
     pin_dot_product_golden,
@@ -407,4 +449,6 @@ ALL_PINS = [
     pin_cross_is_padded_self,
     pin_cross_causal_alignment,
     pin_cross_gqa_uniform_keys,
+    pin_bf16_decoder,
+    pin_bf16_agrees_with_f16_on_common_values,
 ]

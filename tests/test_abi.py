@@ -136,9 +136,10 @@ def test_noalloc_scratch_limit(lib):
                                         None) == _lib.ATTN_ERR_INVALID_ARG
 
 
-def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=64, scale=0.125,
-            causal=0, kl=None, path=0):
-    return lib.attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, kl, path, None)
+def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=64, dtype=0,
+            scale=0.125, causal=0, kl=None, path=0):
+    return lib.attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, dtype, scale, causal, kl, path,
+                           None)
 
 
 @pytest.mark.parametrize("kw,expected", [
@@ -152,6 +153,10 @@ def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=6
     (dict(path=_lib.PATH_SHORT, d=32), _lib.ATTN_ERR_UNSUPPORTED),            # cross shape
     (dict(path=_lib.PATH_SHORT, d=32, Nk=8), _lib.ATTN_ERR_UNSUPPORTED),      # grouped heads
     (dict(v=A + 8), _lib.ATTN_ERR_MISALIGNED),
+    (dict(dtype=2), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=-1), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=_lib.DTYPE_BF16, path=_lib.PATH_WARP_MMA), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=_lib.DTYPE_BF16, Hkv=4, Nk=8, d=32, path=_lib.PATH_SHORT), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(B=1 << 17, H=1 << 10, Hkv=1 << 10, Nq=8, Nk=1 << 30, d=128), _lib.ATTN_ERR_INVALID_ARG),
 ])
 def test_fwd_ex_validation(lib, kw, expected):
@@ -160,12 +165,14 @@ def test_fwd_ex_validation(lib, kw, expected):
 
 def test_splitkv_ex_validation(lib):
     need = lib.attn_splitkv_workspace_bytes(1, 4, 8, 64, 2)
-    args = (A, A, A, A, None, 1, 4, 2, 8, 32, 64, 0.125, 0, None)
+    args = (A, A, A, A, None, 1, 4, 2, 8, 32, 64, 0, 0.125, 0, None)
     assert lib.attn_fwd_splitkv_ex(*args, 2, None, need, None) == _lib.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_splitkv_ex(*args, 2, A, need - 1, None) == _lib.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_splitkv_ex(*args, 17, A, 1 << 30, None) == _lib.ATTN_ERR_INVALID_ARG
-    bad = (A, A, A, A, None, 1, 4, 3, 8, 32, 64, 0.125, 0, None)
+    bad = (A, A, A, A, None, 1, 4, 3, 8, 32, 64, 0, 0.125, 0, None)
     assert lib.attn_fwd_splitkv_ex(*bad, 2, A, 1 << 30, None) == _lib.ATTN_ERR_INVALID_ARG
+    bad_dtype = (A, A, A, A, None, 1, 4, 2, 8, 32, 64, 5, 0.125, 0, None)
+    assert lib.attn_fwd_splitkv_ex(*bad_dtype, 2, A, 1 << 30, None) == _lib.ATTN_ERR_UNSUPPORTED
     assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 0, 64, 0) == -1
     assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 32, 48, 0) == -1
     assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 32, 64, 2) == -1

@@ -27,6 +27,10 @@ MUTANTS = {
                                 "if (1)\n            l += exp(s[j] - m);"),
     "decoder_bias": ("mag = ldexp((double)(1024 + f), e - 25);", "mag = ldexp((double)(1024 + f), e - 24);"),
     "subnormal_scale": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
+    "bf16_exponent_bias": ("mag = ldexp((double)(128 + f), e - 134);",
+                           "mag = ldexp((double)(128 + f), e - 133);"),
+    "bf16_subnormal_scale": ("mag = ldexp((double)f, -133);", "mag = ldexp((double)f, -134);"),
+    "bf16_read_as_f16": ("J.dec = dtype == 1 ? g_bf16_table : g_half_table;", "J.dec = g_half_table;"),
 }
 
 

@@ -14,17 +14,18 @@ from parity import compare, ensure_built, oracle_full, sample_rows, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_splitkv(q, k, v, *, causal, key_lengths=None, sm_scale=None, n_splits=0):
+def run_splitkv(q, k, v, *, causal, key_lengths=None, sm_scale=None, n_splits=0, dtype="f16"):
     """attn_fwd_splitkv on device copies; O and lse sit inside guarded, NaN-prefilled buffers."""
     ensure_built()
     B, H, N, d = q.shape
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(d)
-    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    qd, kd, vd = to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype)
     kld = to_dev(key_lengths)
     pad_o, pad_l = 4096, 1024
     n_o, n_l = q.size, B * H * N
-    o_buf = torch.full((n_o + 2 * pad_o,), float("nan"), dtype=torch.float16, device="cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    o_buf = torch.full((n_o + 2 * pad_o,), float("nan"), dtype=tdt, device="cuda")
     l_buf = torch.full((n_l + 2 * pad_l,), float("nan"), dtype=torch.float32, device="cuda")
     o_buf[:pad_o] = 1234.0
     o_buf[pad_o + n_o:] = 1234.0
