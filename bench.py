@@ -501,7 +501,8 @@ def split_kv(torch, api, peaks, peak_src):
 
 
 def to_host(torch, x, dtype):
-    """numpy -> CPU tensor (uint16 bit patterns become torch.bfloat16 for bf16)."""
+    """numpy -> CPU tensor (uint16 bit patterns become torch.bfloat16 for bf16; float16 and
+    float32 arrays keep their type)."""
     import numpy as np
     if dtype == "bf16":
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
@@ -539,6 +540,26 @@ def variants(torch, api, peaks, peak_src):
                                   "unit": "TFLOP/s", "frac": tf / peak,
                                   "peak_source": f"{peak_src} bf16 dense burst"}}
         del qd, kd, vd, od
+    # fp32 inputs at the reranking shape: HBM-bound, GB/s of Q, K, V read and O written once
+    w = synth.WORKLOADS["rerank_f32"]
+    q, k, v, kl = synth.draw_workload(w)
+    qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
+    kld = torch.from_numpy(kl).cuda()
+    od = torch.empty_like(qd)
+
+    def fn32():
+        api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od)
+
+    time_launches(torch, fn32, 3, flush)
+    ms = statistics.median(time_launches(torch, fn32, 30, flush))
+    nbytes = 2 * synth.min_bytes(w.B, w.H, w.N, w.d) + kl.nbytes  # fp32: twice the fp16 bytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    out["rerank_f32"] = {"workload": w.describe(), "value": gbs, "unit": "GB/s", "launch_ms": ms,
+                         "bytes": nbytes, "kernel": "tcgen05", "dtype": "f32 (TF32 products)",
+                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                      "frac": gbs / hbm, "peak_source": f"{peak_src} copy bandwidth"},
+                         "timing": "single launches, each after the L2 flush (launch latency included)"}
     out["l2"] = "flushed (512 MiB write) before every timed launch"
     return out
 

@@ -17,6 +17,7 @@ ATTN_ERR_SCRATCH_LIMIT = 6
 
 DTYPE_F16 = 0
 DTYPE_BF16 = 1
+DTYPE_F32 = 2
 
 PATH_AUTO = 0
 PATH_WARP_MMA = 1

@@ -31,8 +31,9 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
         sm_scale: float | None = None, key_lengths: torch.Tensor | None = None,
         return_lse: bool = False, out: torch.Tensor | None = None,
         lse_out: torch.Tensor | None = None, path: str = "auto"):
-    """O = softmax(sm_scale * Q K^T + mask) V for fp16 or bf16 tensors (q, k, v and out of one
-    dtype; bf16 runs on the tcgen05 kernel): q [B, H, N, d] and k, v of the same shape
+    """O = softmax(sm_scale * Q K^T + mask) V for fp16, bf16 or fp32 tensors (q, k, v and out of
+    one dtype; bf16 and fp32 run on the tcgen05 kernel, fp32 with d = 32 and TF32 products):
+    q [B, H, N, d] and k, v of the same shape
     (self-attention) or [B, H_kv, N_k, d] (cross-attention and grouped-query attention: H a
     multiple of H_kv, query head h reads key/value head h // (H // H_kv)).
 
@@ -94,7 +95,9 @@ def _dtype_code(q):
         return _lib.DTYPE_F16
     if q.dtype == torch.bfloat16:
         return _lib.DTYPE_BF16
-    raise TypeError(f"q must be torch.float16 or torch.bfloat16, got {q.dtype}")
+    if q.dtype == torch.float32:
+        return _lib.DTYPE_F32
+    raise TypeError(f"q must be torch.float16, torch.bfloat16 or torch.float32, got {q.dtype}")
 
 
 def _shapes(q, k):

@@ -60,7 +60,9 @@ attn_status_t validate(const void *q, const void *k, const void *v, const void *
         return ATTN_ERR_INVALID_ARG;
     if (sh.d != 32 && sh.d != 64 && sh.d != 128)
         return ATTN_ERR_UNSUPPORTED;
-    if (sh.dtype != ATTN_DTYPE_F16 && sh.dtype != ATTN_DTYPE_BF16)
+    if (sh.dtype != ATTN_DTYPE_F16 && sh.dtype != ATTN_DTYPE_BF16 && sh.dtype != ATTN_DTYPE_F32)
+        return ATTN_ERR_UNSUPPORTED;
+    if (sh.dtype == ATTN_DTYPE_F32 && sh.d != 32) // fp32 inputs: head dimension 32 only
         return ATTN_ERR_UNSUPPORTED;
     const int64_t bh = static_cast<int64_t>(sh.B) * sh.H;
     if (bh > INT32_MAX)
@@ -92,7 +94,9 @@ attn::FwdParams make_params(const void *q, const void *k, const void *v, void *o
     p.d = sh.d;
     p.Hkv = sh.Hkv;
     p.Nk = sh.Nk;
-    p.dtype = sh.dtype == ATTN_DTYPE_BF16 ? attn::kDtypeBF16 : attn::kDtypeF16;
+    p.dtype = sh.dtype == ATTN_DTYPE_BF16 ? attn::kDtypeBF16
+              : sh.dtype == ATTN_DTYPE_F32 ? attn::kDtypeF32
+                                           : attn::kDtypeF16;
     p.sm_scale = sm_scale;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.causal = causal;
@@ -147,11 +151,11 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
         path != ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
-    // The short-sequence kernel serves fp16 self-attention only; bf16 runs on the tiled
-    // tcgen05 kernel only.
+    // The short-sequence kernel serves fp16 self-attention only; bf16 and fp32 run on the
+    // tiled tcgen05 kernel only.
     if (path == ATTN_PATH_SHORT && (!sh.self() || sh.Nq > 256 || sh.d > 64))
         return ATTN_ERR_UNSUPPORTED;
-    if (sh.dtype == ATTN_DTYPE_BF16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05)
+    if (sh.dtype != ATTN_DTYPE_F16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05)
         return ATTN_ERR_UNSUPPORTED;
     if (path == ATTN_PATH_AUTO)
         path = (sh.self() && sh.dtype == ATTN_DTYPE_F16) ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;

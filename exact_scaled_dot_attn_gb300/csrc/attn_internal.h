@@ -8,16 +8,17 @@
 
 namespace attn {
 
-// Element type of Q, K, V and O (16-bit storage; __half pointers below hold either).
+// Element type of Q, K, V and O (the __half pointers below hold any of them).
 constexpr int kDtypeF16 = 0;
 constexpr int kDtypeBF16 = 1; // tcgen05 kernels only
+constexpr int kDtypeF32 = 2;  // fp32 in and out, tf32 tensor-core products: tcgen05 kernel, d = 32
 
 struct FwdParams {
     const __half *q;
     const __half *k;
     const __half *v;
     __half *o;
-    int dtype;                  // kDtypeF16 or kDtypeBF16
+    int dtype;                  // kDtypeF16, kDtypeBF16 or kDtypeF32
     float *lse;                 // may be null
     const int32_t *key_lengths; // may be null
     int B, H, N, d; // N: query rows per head

@@ -117,14 +117,28 @@ template <int D> struct RegSplit {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f; // lazy-correction threshold (log2 units)
 
-template <int D> struct Cfg {
-    static constexpr int kBoxCols = D < 64 ? D : 64;   // columns per TMA box = one swizzle row
-    static constexpr int kRowBytes = kBoxCols * 2;     // 64 B (d = 32) or 128 B
+// Element kinds of Q, K, V and O: fp16 and bf16 run tcgen05.mma kind::f16; fp32 inputs run
+// kind::tf32 (the tensor core reads 10 fraction bits of each fp32 value).
+constexpr int kKindF16 = 0;
+constexpr int kKindBF16 = 1;
+constexpr int kKindTF32 = 2;
+template <int KIND> __host__ __device__ constexpr int elem_bytes() { return KIND == kKindTF32 ? 4 : 2; }
+
+// Tile geometry for head dimension D and ES-byte elements. A TMA box row is one swizzle row
+// (64 bytes for fp16 at d = 32, 128 bytes otherwise); fp32 at d = 32 has the byte geometry of
+// fp16 at d = 64.
+template <int D, int ES = 2> struct Cfg {
+    static constexpr int kBoxCols = D * ES < 128 ? D : 128 / ES; // elements per TMA box row
+    static constexpr int kRowBytes = kBoxCols * ES;     // 64 B or 128 B
     static constexpr int kBoxBytes = kBM * kRowBytes;  // one 128-row box
-    static constexpr int kTileBytes = kBM * D * 2;     // a 128 x D fp16 tile (D / kBoxCols boxes)
-    static constexpr uint32_t kSwizzle = D < 64 ? 4u : 2u; // descriptor layout: 64 B / 128 B swizzle
-    static constexpr int kQStages = D == 128 ? 1 : 2;      // Q0/Q1 buffers (2: next unit prefetched)
-    static constexpr int kStages = D == 128 ? 5 : (D == 64 ? 9 : 16); // K/V ring depth
+    static constexpr int kTileBytes = kBM * D * ES;    // a 128 x D tile (D / kBoxCols boxes)
+    static constexpr uint32_t kSwizzle = kRowBytes < 128 ? 4u : 2u; // descriptor layout: 64 B / 128 B swizzle
+    static constexpr int kKStep = 32 / ES;             // K elements per MMA instruction (32 bytes)
+    static constexpr int kQStages = kTileBytes >= 32768 ? 1 : 2; // Q0/Q1 buffers (2: next unit prefetched)
+    // fp32 (tf32) tiles: the PV product needs V K-major (tf32 operands cannot be MN-major), so
+    // each V tile is transposed into one of kVTStages V^T buffers, taking two ring stages' room.
+    static constexpr int kVTStages = ES == 4 ? 2 : 0;
+    static constexpr int kStages = ES == 4 ? 7 : (kTileBytes >= 32768 ? 5 : (kTileBytes >= 16384 ? 9 : 16)); // K/V ring
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
     // O accumulators: two per Q tile when they fit (d <= 64), so that a unit's epilogue
     // can read one while the next unit's PV products accumulate into the other.
@@ -136,7 +150,8 @@ template <int D> struct Cfg {
     }
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kQStages * 2 * kTileBytes;
-    static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+    static constexpr int kOffVT = kOffKV + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffVT + kVTStages * kTileBytes;
     static constexpr int kSmemBytes = kOffBar + 1024 + 1024; // barriers + alignment slack
 };
 
@@ -277,17 +292,21 @@ __device__ __forceinline__ bool stream_take(UnitStream &st, const TcArgs &a, con
 }
 
 // Barrier block layout (8 bytes each).
-template <int D> struct Bars {
-    static constexpr int kQFull = 0;                              // [kQStages]
-    static constexpr int kQEmpty = kQFull + Cfg<D>::kQStages;     // [kQStages]
-    static constexpr int kKVFull = kQEmpty + Cfg<D>::kQStages;
-    static constexpr int kKVEmpty = kKVFull + Cfg<D>::kStages;
-    static constexpr int kSFull = kKVEmpty + Cfg<D>::kStages; // [2]
+template <int D, int ES = 2> struct Bars {
+    static constexpr int kQFull = 0;                                  // [kQStages]
+    static constexpr int kQEmpty = kQFull + Cfg<D, ES>::kQStages;     // [kQStages]
+    static constexpr int kKVFull = kQEmpty + Cfg<D, ES>::kQStages;
+    static constexpr int kKVEmpty = kKVFull + Cfg<D, ES>::kStages;
+    static constexpr int kSFull = kKVEmpty + Cfg<D, ES>::kStages; // [2]
     static constexpr int kPFull = kSFull + 2;                 // [2]
     static constexpr int kOReady = kPFull + 2;                // [tile * 2 + O buffer]
     static constexpr int kOEmpty = kOReady + 4;               // [tile * 2 + O buffer]
     static constexpr int kMmaDone = kOEmpty + 4;
-    static constexpr int kCount = kMmaDone + 1;
+    // tf32 only: V tile landed (MMA warp -> transposer warps), V^T written, V^T buffer free
+    static constexpr int kVReady = kMmaDone + 1;  // [2]
+    static constexpr int kVTFull = kVReady + 2;   // [2]
+    static constexpr int kVTEmpty = kVTFull + 2;  // [2]
+    static constexpr int kCount = kVTEmpty + 2;
 };
 
 // Column chunks of the S row: the allowed columns of a row are a prefix e < lim (key
@@ -342,10 +361,11 @@ __device__ __forceinline__ float row_max_full(const uint32_t (&sv)[kBN], float s
     return min3(min3(acc[0], acc[1], acc[2]), min3(acc[3], acc[4], acc[5]), fminf(acc[6], acc[7])) * scale;
 }
 
-// p_e = 2^(S_e * scale - m) over a fully allowed row, rounded to fp16 pairs and stored to
-// TMEM at tP in two halves of 32 columns; returns sum_e p_e in fp32 (f32x2 arithmetic).
-template <bool BF16>
-__device__ __forceinline__ float exp_pack_full(const uint32_t (&sv)[kBN], float scale, float neg_m,
+// p_e = 2^(S_e * scale - m) over a fully allowed row, stored to TMEM at tP: rounded to
+// 16-bit pairs (fp16 or bf16) in two halves of 32 columns, or (tf32) as fp32 in 128 columns
+// over the row's own scores; returns sum_e p_e in fp32 (f32x2 arithmetic).
+template <int KIND>
+__device__ __forceinline__ float exp_pack_full(uint32_t (&sv)[kBN], float scale, float neg_m,
                                                uint32_t tP)
 {
     const uint64_t sc2 = f2_pack(scale, scale);
@@ -354,24 +374,46 @@ __device__ __forceinline__ float exp_pack_full(const uint32_t (&sv)[kBN], float 
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         acc[i] = f2_pack(0.f, 0.f);
+    if constexpr (KIND == kKindTF32) {
+        // each p replaces its own score in sv (no second 128-value array)
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+        for (int c = 0; c < kBN / 32; ++c) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-            const int e = half * 64 + i;
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-            pk[i >> 1] = pack2<BF16>(p0, p1);
+            for (int i = 0; i < 32; i += 2) {
+                const int e = c * 32 + i;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+                sv[e] = __float_as_uint(p0);
+                sv[e + 1] = __float_as_uint(p1);
+            }
+            tmem_st32(tP + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&sv[c * 32]));
         }
-        tmem_st32(tP + half * 32, pk);
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+        return (a0 + a1) + (b0 + b1);
+    } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                const int e = half * 64 + i;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+                pk[i >> 1] = pack2<KIND == kKindBF16>(p0, p1);
+            }
+            tmem_st32(tP + half * 32, pk);
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+        return (a0 + a1) + (b0 + b1);
     }
-    float a0, a1, b0, b1;
-    f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
-    f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-    return (a0 + a1) + (b0 + b1);
 }
 
 // Row max of the scaled scores x_e = S_e * scale over the allowed columns e < lim
@@ -397,12 +439,13 @@ __device__ __forceinline__ float row_max(const uint32_t (&sv)[kBN], float scale,
     return m;
 }
 
-// p_e = 2^(S_e * scale - m) for the allowed columns e < lim, 0 elsewhere, rounded to fp16
-// pairs and stored to TMEM at tP (two halves of 32 columns, so only half of the packed
-// row is held in registers at a time); returns sum_e p_e in fp32. Pairs of lanes use
-// f32x2 arithmetic; fully masked chunks store zeros without evaluating any exponential.
-template <bool BF16>
-__device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale, float neg_m, int lim,
+// p_e = 2^(S_e * scale - m) for the allowed columns e < lim, 0 elsewhere, stored to TMEM at
+// tP as exp_pack_full stores it (16-bit pairs in two halves of 32 columns, so only half of the
+// packed row is held in registers at a time, or fp32 for tf32); returns sum_e p_e in fp32.
+// Pairs of lanes use f32x2 arithmetic; fully masked chunks store zeros without evaluating any
+// exponential.
+template <int KIND>
+__device__ __forceinline__ float exp_pack(uint32_t (&sv)[kBN], float scale, float neg_m, int lim,
                                           uint32_t tP)
 {
     const uint64_t sc2 = f2_pack(scale, scale);
@@ -411,12 +454,11 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         acc[i] = f2_pack(0.f, 0.f);
+    if constexpr (KIND == kKindTF32) {
+        // each p replaces its own score in sv (no second 128-value array)
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c = half * 2 + cc;
+        for (int c = 0; c < kBN / kChunkCols; ++c) {
+            uint32_t(&pv)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[c * kChunkCols]);
             if (lim >= (c + 1) * kChunkCols) {
 #pragma unroll
                 for (int i = 0; i < kChunkCols; i += 2) {
@@ -425,7 +467,8 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
                     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                     acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-                    pk[cc * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
+                    pv[i] = __float_as_uint(p0);
+                    pv[i + 1] = __float_as_uint(p1);
                 }
             } else if (lim > c * kChunkCols) {
 #pragma unroll
@@ -436,41 +479,89 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sv)[kBN], float scale
                     const float p0 = e < lim ? ex2_approx(x0) : 0.f;
                     const float p1 = e + 1 < lim ? ex2_approx(x1) : 0.f;
                     acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-                    pk[cc * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
+                    pv[i] = __float_as_uint(p0);
+                    pv[i + 1] = __float_as_uint(p1);
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[cc * 16 + i] = 0u;
+                for (int i = 0; i < 32; ++i)
+                    pv[i] = 0u;
             }
+            tmem_st32(tP + c * 32, pv);
         }
-        tmem_st32(tP + half * 32, pk);
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+        return (a0 + a1) + (b0 + b1);
+    } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = half * 2 + cc;
+                if (lim >= (c + 1) * kChunkCols) {
+#pragma unroll
+                    for (int i = 0; i < kChunkCols; i += 2) {
+                        const int e = c * kChunkCols + i;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+                        pk[cc * 16 + (i >> 1)] = pack2<KIND == kKindBF16>(p0, p1);
+                    }
+                } else if (lim > c * kChunkCols) {
+#pragma unroll
+                    for (int i = 0; i < kChunkCols; i += 2) {
+                        const int e = c * kChunkCols + i;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), x0, x1);
+                        const float p0 = e < lim ? ex2_approx(x0) : 0.f;
+                        const float p1 = e + 1 < lim ? ex2_approx(x1) : 0.f;
+                        acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+                        pk[cc * 16 + (i >> 1)] = pack2<KIND == kKindBF16>(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[cc * 16 + i] = 0u;
+                }
+            }
+            tmem_st32(tP + half * 32, pk);
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+        return (a0 + a1) + (b0 + b1);
     }
-    float a0, a1, b0, b1;
-    f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
-    f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-    return (a0 + a1) + (b0 + b1);
 }
 
-// BF16: Q, K, V, O (and P) are bf16 instead of fp16.
-template <int D, bool SPLIT, bool BF16>
+// KIND: element kind of Q, K, V and O (kKindF16, kKindBF16, or kKindTF32 for fp32 inputs and
+// output); P has the kind of the inputs (one MMA takes A and B of one type).
+template <int D, bool SPLIT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tcgen05_kernel(const TcArgs args, const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ SchedTable sched)
 {
-    using C = Cfg<D>;
-    using BB = Bars<D>;
+    constexpr bool TF32 = KIND == kKindTF32;
+    constexpr int kES = elem_bytes<KIND>();
+    using C = Cfg<D, kES>;
+    using BB = Bars<D, kES>;
     // S = Q K^T: both K-major; O += P V: P from TMEM, V MN-major. A and B share one type.
-    constexpr uint32_t kIdescS = idesc_f16_f32(kBM, kBN, 0, 0, BF16);
-    constexpr uint32_t kIdescPV = idesc_f16_f32(kBM, D, 0, 1, BF16);
+    constexpr uint32_t kIdescS = TF32 ? idesc_tf32_f32(kBM, kBN, 0, 0)
+                                      : idesc_f16_f32(kBM, kBN, 0, 0, KIND == kKindBF16);
+    // (tf32: V is first transposed to K-major V^T, tf32 operands cannot be MN-major)
+    constexpr uint32_t kIdescPV = TF32 ? idesc_tf32_f32(kBM, D, 0, 0)
+                                       : idesc_f16_f32(kBM, D, 0, 1, KIND == kKindBF16);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw_addr);
     const uint32_t sQ = base + C::kOffQ;
     const uint32_t sKV = base + C::kOffKV;
+    const uint32_t sVT = base + C::kOffVT;
     const uint32_t sBar = base + C::kOffBar;
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * BB::kCount);
@@ -504,6 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(BB::kOEmpty + i), kBM);
         }
         mbar_init(bar(BB::kMmaDone), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BB::kVReady + i), 1);
+            mbar_init(bar(BB::kVTFull + i), 64); // the 64 threads of the transposer warps
+            mbar_init(bar(BB::kVTEmpty + i), 1);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -593,6 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         setmaxnreg_dec<RegSplit<D>::kControl>();
         uint32_t q_it = 0, kv_it = 0;
+        uint32_t vt_it = 0; // V tiles consumed (tf32: V^T buffer vt_it & 1)
         // Phase parities kept as bit masks (no runtime-indexed local arrays):
         uint32_t p_par = 0;  // bit t: parity of the P-ready waits of tile t
         uint32_t oe_par = 0; // bit t*2+b: parity of the uses of O buffer b of tile t
@@ -616,32 +713,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto desc = [](uint32_t lo) -> uint64_t {
             return (static_cast<uint64_t>(kDescHi) << 32) | lo;
         };
-        // S_t = Q_t K^T: K-major operands, 16 columns (32 bytes) per k-step inside a
-        // swizzle row, a new box every kBoxCols / 16 steps. (Issued by the elected lane.)
+        // S_t = Q_t K^T: K-major operands, 32 bytes (16 fp16 / 8 fp32 elements) per k-step
+        // inside a swizzle row, a new box every kBoxCols / kKStep steps. (Issued by the
+        // elected lane.)
         auto issue_s = [&](int t, uint32_t k_slot) {
             const uint32_t qlo = ((sQ + (q_slot * 2 + t) * C::kTileBytes) >> 4) | kLboK;
             const uint32_t klo = ((sKV + k_slot * C::kTileBytes) >> 4) | kLboK;
             const uint32_t d_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
-            constexpr int kStepsPerBox = C::kBoxCols / 16;
+            constexpr int kStepsPerBox = C::kBoxCols / C::kKStep;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < D / C::kKStep; ++kk) {
                 constexpr int kBox16 = C::kBoxBytes >> 4;
                 const uint32_t off = (kk / kStepsPerBox) * kBox16 + (kk % kStepsPerBox) * 2;
-                mma_ss(d_tmem, desc(qlo + off), desc(klo + off), kIdescS, kk > 0 ? 1u : 0u);
+                if constexpr (TF32)
+                    mma_ss_tf32(d_tmem, desc(qlo + off), desc(klo + off), kIdescS, kk > 0 ? 1u : 0u);
+                else
+                    mma_ss(d_tmem, desc(qlo + off), desc(klo + off), kIdescS, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar(BB::kSFull + t));
         };
-        // O_t += P_t V: P from TMEM (8 columns = 16 fp16 keys per k-step); V is MN-major,
-        // 16 keys (rows) per k-step. (Issued by the elected lane.)
-        auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
-            const uint32_t vlo = ((sKV + v_slot * C::kTileBytes) >> 4) | kLboV;
+        // O_t += P_t V: P from TMEM (8 columns per k-step: 16 packed 16-bit keys, or 8 fp32
+        // keys). 16-bit: V is MN-major, kKStep keys (rows) per k-step. tf32: V^T (buffer vt) is
+        // K-major in four 32-key blocks of 4 KB, 8 keys (32 bytes) per k-step. (Issued by the
+        // elected lane.)
+        auto issue_pv = [&](int t, uint32_t v_slot, uint32_t vt, bool accumulate) {
             const uint32_t a_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
             const int b = static_cast<int>((ob >> t) & 1u);
             const uint32_t d_tmem = tmem + C::tmem_o(t, b);
+            if constexpr (TF32) {
+                const uint32_t vtlo = ((sVT + vt * C::kTileBytes) >> 4) | kLboK;
+                constexpr uint32_t kBlock16 = (32u * D * 4u) >> 4; // one 32-key block of V^T
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((16 * C::kRowBytes) >> 4)),
-                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBN / C::kKStep; ++kk)
+                    mma_ts_tf32(d_tmem, a_tmem + kk * 8, desc(vtlo + (kk / 4) * kBlock16 + (kk % 4) * 2),
+                                kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            } else {
+                const uint32_t vlo = ((sKV + v_slot * C::kTileBytes) >> 4) | kLboV;
+#pragma unroll
+                for (int kk = 0; kk < kBN / C::kKStep; ++kk)
+                    mma_ts(d_tmem, a_tmem + kk * 8, desc(vlo + kk * ((C::kKStep * C::kRowBytes) >> 4)),
+                           kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            }
             mma_commit(bar(BB::kOReady + t * 2 + b));
         };
         UnitStream us;
@@ -693,6 +805,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(bar(BB::kKVFull + v_slot), (kv_it / C::kStages) & 1u))
                     break;
                 ++kv_it;
+                const uint32_t vt = vt_it & 1u; // tf32: the V^T buffer of this V tile
+                if constexpr (TF32) {
+                    // hand V_j to the transposer warps (in order, so their waits never alias)
+                    if (elect_one())
+                        mbar_arrive(bar(BB::kVReady + vt));
+                    __syncwarp();
+                }
+                bool vt_ready = false;
                 const bool has_next = j + 1 < U.n_kv;
                 bool k_ready = false;
                 uint32_t k_slot = 0;
@@ -709,9 +829,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait(bar(BB::kPFull + t), (p_par >> t) & 1u))
                         break;
                     p_par ^= 1u << t;
+                    if constexpr (TF32) {
+                        if (!vt_ready) {
+                            if (!wait(bar(BB::kVTFull + vt), (vt_it >> 1) & 1u))
+                                break;
+                            vt_ready = true;
+                        }
+                    }
                     tc_fence_after();
                     if (elect_one())
-                        issue_pv(t, v_slot, j > 0);
+                        issue_pv(t, v_slot, vt, j > 0);
                     __syncwarp();
                     if (j + 1 < kv_tiles(U, t)) {
                         if (!k_ready) {
@@ -731,6 +858,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 if (elect_one()) {
                     mma_commit(bar(BB::kKVEmpty + v_slot));
+                    if constexpr (TF32)
+                        mma_commit(bar(BB::kVTEmpty + vt));
                     if (has_next) {
                         // the tile with the most K/V tiles always consumed K_{j+1} above
                         mma_commit(bar(BB::kKVEmpty + k_slot));
@@ -739,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
+                ++vt_it;
                 if (!has_next && have_next) {
                     if (!start_unit(Un))
                         break;
@@ -758,7 +888,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(BB::kMmaDone), 0, nullptr, kWaitLimitNs);
         __syncwarp();
     } else if (warp >= 8) {
-        setmaxnreg_dec<RegSplit<D>::kControl>(); // idle warps of the control warpgroup
+        setmaxnreg_dec<RegSplit<D>::kControl>(); // warps 10 and 11 of the control warpgroup
+        if constexpr (TF32) {
+            // ------------------------------------------------------------ V transposer (tf32)
+            // V_j [128 keys x D] (TMA layout: 128-byte rows, 128-byte swizzle) -> V^T [D x 128
+            // keys], K-major: four 32-key blocks of D rows x 128 bytes, same swizzle. Each
+            // thread moves four 4 x 4 blocks (four 16-byte loads, a register transpose, four
+            // 16-byte stores). V_j's stage is known in order from the MMA warp (VReady), so
+            // no wait here can mistake an old phase for a new one.
+            static_assert(D == 32, "the tf32 path is built for d = 32");
+            const int tt = static_cast<int>(threadIdx.x) - 10 * 32; // 0..63
+            uint32_t g = 0; // V tiles transposed
+            bool ok = true;
+            UnitStream us;
+            stream_init(us, args, sched);
+            Unit U;
+            while (ok && stream_take(us, args, sched, U)) {
+                for (int j = 0; j < U.n_kv; ++j) {
+                    const uint32_t vt = g & 1u, use = g >> 1;
+                    if (!warp_wait(bar(BB::kVReady + vt), use & 1u) ||
+                        !warp_wait(bar(BB::kVTEmpty + vt), (use & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t kv = 2 * g + 1; // K and V tiles alternate in the ring
+                    const unsigned char *src = smem + C::kOffKV + (kv % C::kStages) * C::kTileBytes;
+                    unsigned char *dst = smem + C::kOffVT + vt * C::kTileBytes;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int blk = tt + 64 * i;
+                        const int rb = blk >> 3, cb = blk & 7; // keys 4rb.., dims 4cb..
+                        float4 x[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int key = 4 * rb + r;
+                            x[r] = *reinterpret_cast<const float4 *>(src + key * 128 + ((cb ^ (key & 7)) << 4));
+                        }
+                        const float4 y[4] = {make_float4(x[0].x, x[1].x, x[2].x, x[3].x),
+                                             make_float4(x[0].y, x[1].y, x[2].y, x[3].y),
+                                             make_float4(x[0].z, x[1].z, x[2].z, x[3].z),
+                                             make_float4(x[0].w, x[1].w, x[2].w, x[3].w)};
+#pragma unroll
+                        for (int n = 0; n < 4; ++n) {
+                            const int dim = 4 * cb + n;
+                            *reinterpret_cast<float4 *>(dst + (rb >> 3) * (32 * D * 4) + dim * 128 +
+                                                        (((rb & 7) ^ (dim & 7)) << 4)) = y[n];
+                        }
+                    }
+                    // the writes are read by tcgen05.mma (async proxy)
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                    mbar_arrive(bar(BB::kVTFull + vt));
+                    ++g;
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
         setmaxnreg_inc<RegSplit<D>::kSoftmax>();
@@ -821,6 +1004,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     args.lpart[r] = pe.l > 0.f ? (pe.m_ref + log2f(pe.l)) * kLn2 : -INFINITY;
                 return true;
             }
+            if constexpr (TF32) {
+                // fp32 output: O / l as it is
+                float4 *orow = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) +
+                                                          (static_cast<size_t>(pe.bh) * p.N + pe.row) * D);
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c0, ov);
+                    if (pe.row < p.N) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            orow[(c0 + e) >> 2] = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                                              __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(BB::kOEmpty + t * 2 + pe.b));
+                if (p.lse && pe.row < p.N)
+                    p.lse[static_cast<size_t>(pe.bh) * p.N + pe.row] =
+                        pe.l > 0.f ? (pe.m_ref + log2f(pe.l)) * kLn2 : -INFINITY;
+                return true;
+            }
             __half *orow = p.o + (static_cast<size_t>(pe.bh) * p.N + pe.row) * D;
             constexpr int kChunk = D < 64 ? D : 64; // O columns per TMEM load
 #pragma unroll
@@ -833,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t h[kChunk / 2];
 #pragma unroll
                 for (int e = 0; e < kChunk; e += 2)
-                    h[e >> 1] = pack2<BF16>(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+                    h[e >> 1] = pack2<KIND == kKindBF16>(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
                 if (pe.row < p.N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
 #pragma unroll
@@ -867,10 +1072,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
                     args.lpart[r] = -INFINITY;
                 } else if (row < p.N) {
+                    // D elements of kES bytes: D * kES / 16 vectors of 16 bytes
                     uint4 z = make_uint4(0, 0, 0, 0);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(U.bh) * p.N + row) * D);
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<char *>(p.o) +
+                                                           (static_cast<size_t>(U.bh) * p.N + row) * D * kES);
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c)
+                    for (int c = 0; c < D * kES / 16; ++c)
                         dst[c] = z;
                     if (p.lse)
                         p.lse[static_cast<size_t>(U.bh) * p.N + row] = -INFINITY;
@@ -907,8 +1114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
 
                 // P = exp2(S * scale - m_ref) as fp16, written over the first 64 columns of S
-                const float rs = need_mask ? exp_pack<BF16>(sv, scale, neg_m, lim, tS)
-                                           : exp_pack_full<BF16>(sv, scale, neg_m, tS);
+                const float rs = need_mask ? exp_pack<KIND>(sv, scale, neg_m, lim, tS)
+                                           : exp_pack_full<KIND>(sv, scale, neg_m, tS);
                 // O holds the PV products of earlier tiles; rescale it (after the last of
                 // them is done) before this tile's P is released to the MMA warp. The warp
                 // does it together when any of its rows needs it (tcgen05.ld/st are
@@ -978,24 +1185,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// [heads, rows, D] fp16 viewed as a 3-D tensor (D innermost): Q is [B*H, N, D], K and V
-// [B*Hkv, Nk, D]; boxes of 128 rows x 64 columns with a 128-byte swizzle (x 32 columns with
-// a 64-byte swizzle for D = 32); rows past the end read as zero.
-bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, bool bf16)
+// [heads, rows, D] viewed as a 3-D tensor (D innermost): Q is [B*H, N, D], K and V
+// [B*Hkv, Nk, D]; boxes of 128 rows x one swizzle row (128 bytes with a 128-byte swizzle, or
+// 64 bytes with a 64-byte swizzle for fp16 at D = 32); rows past the end read as zero.
+template <int D, int KIND>
+bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N)
 {
+    using C = Cfg<D, elem_bytes<KIND>()>;
     auto enc = tensor_map_encoder();
     if (!enc)
         return false;
-    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt = KIND == kKindTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : KIND == kKindBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    constexpr cuuint64_t kES = elem_bytes<KIND>();
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(D < 64 ? D : 64), static_cast<cuuint32_t>(kBM), 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * kES,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * kES};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(C::kBoxCols), static_cast<cuuint32_t>(kBM), 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE,
-               D < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+               C::kRowBytes < 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1084,18 +1296,18 @@ std::shared_ptr<SchedTable> schedule_for(int BH, int N, int Nk, int causal, int 
     return t;
 }
 
-template <int D, bool SPLIT, bool BF16>
+template <int D, bool SPLIT, int KIND>
 cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpart, cudaStream_t stream,
                      unsigned int *status)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, elem_bytes<KIND>()>;
     const int BH = p.B * p.H;
     if (p.Hkv < 1 || p.H % p.Hkv != 0)
         return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     CUtensorMap mq, mk, mv;
-    if (!encode_map(&mq, p.q, BH, p.N, D, BF16) || !encode_map(&mk, p.k, BHkv, p.Nk, D, BF16) ||
-        !encode_map(&mv, p.v, BHkv, p.Nk, D, BF16))
+    if (!encode_map<D, KIND>(&mq, p.q, BH, p.N) || !encode_map<D, KIND>(&mk, p.k, BHkv, p.Nk) ||
+        !encode_map<D, KIND>(&mv, p.v, BHkv, p.Nk))
         return cudaErrorInvalidValue;
     TcArgs a;
     a.p = p;
@@ -1113,7 +1325,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
     cudaError_t err = device_sm_count(&sms);
     if (err != cudaSuccess)
         return err;
-    auto kernel = attn_fwd_tcgen05_kernel<D, SPLIT, BF16>;
+    auto kernel = attn_fwd_tcgen05_kernel<D, SPLIT, KIND>;
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess)
         return err;
@@ -1136,7 +1348,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
 // logsumexp of range s and O_s its normalised output, lse = log sum_s exp(lse_s) and
 // O = sum_s exp(lse_s - lse) O_s. Ranges without an allowed key (lse_s = -inf) weigh 0; a
 // row with none at all gets O = 0 and lse = -inf.
-template <int D, bool BF16>
+template <int D, int KIND>
 __global__ void __launch_bounds__(256)
     attn_splitkv_merge_kernel(const float *__restrict__ opart, const float *__restrict__ lpart,
                               __half *__restrict__ o, float *__restrict__ lse, long long rows, int S)
@@ -1170,20 +1382,22 @@ __global__ void __launch_bounds__(256)
             acc[c] += w * src[c];
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    // O (16-bit elements: bf16 when BF16, fp16 otherwise), rounded to nearest even
-    __half *dst = o + row * D + lane * kPer;
+    // O: fp32 for KIND tf32, else bf16 or fp16 rounded to nearest even
+    const long long e0 = row * D + lane * kPer;
 #pragma unroll
     for (int c = 0; c < kPer; ++c) {
-        if constexpr (BF16)
-            reinterpret_cast<__nv_bfloat16 *>(dst)[c] = __float2bfloat16_rn(acc[c] * inv);
+        if constexpr (KIND == kKindTF32)
+            reinterpret_cast<float *>(o)[e0 + c] = acc[c] * inv;
+        else if constexpr (KIND == kKindBF16)
+            reinterpret_cast<__nv_bfloat16 *>(o)[e0 + c] = __float2bfloat16_rn(acc[c] * inv);
         else
-            dst[c] = __float2half_rn(acc[c] * inv);
+            o[e0 + c] = __float2half_rn(acc[c] * inv);
     }
     if (lse && lane == 0)
         lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
-template <int D, bool BF16>
+template <int D, int KIND>
 cudaError_t launch_merge(const FwdParams &p, int n_splits, const float *opart, const float *lpart,
                          cudaStream_t stream)
 {
@@ -1191,7 +1405,7 @@ cudaError_t launch_merge(const FwdParams &p, int n_splits, const float *opart, c
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    attn_splitkv_merge_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    attn_splitkv_merge_kernel<D, KIND><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         opart, lpart, p.o, p.lse, rows, n_splits);
     return cudaGetLastError();
 }
@@ -1200,34 +1414,49 @@ cudaError_t launch_merge(const FwdParams &p, int n_splits, const float *opart, c
 
 namespace {
 
-template <bool BF16>
+template <int KIND>
 cudaError_t launch_tcgen05_t(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
-    switch (p.d) {
-    case 32: return launch_d<32, false, BF16>(p, 1, nullptr, nullptr, stream, status);
-    case 64: return launch_d<64, false, BF16>(p, 1, nullptr, nullptr, stream, status);
-    case 128: return launch_d<128, false, BF16>(p, 1, nullptr, nullptr, stream, status);
-    default: return cudaErrorInvalidValue;
+    if constexpr (KIND == kKindTF32) {
+        // fp32 inputs: head dimension 32 only
+        return p.d == 32 ? launch_d<32, false, KIND>(p, 1, nullptr, nullptr, stream, status)
+                         : cudaErrorInvalidValue;
+    } else {
+        switch (p.d) {
+        case 32: return launch_d<32, false, KIND>(p, 1, nullptr, nullptr, stream, status);
+        case 64: return launch_d<64, false, KIND>(p, 1, nullptr, nullptr, stream, status);
+        case 128: return launch_d<128, false, KIND>(p, 1, nullptr, nullptr, stream, status);
+        default: return cudaErrorInvalidValue;
+        }
     }
 }
 
-template <bool BF16>
+template <int KIND>
 cudaError_t launch_splitkv_t(const FwdParams &p, int n_splits, float *opart, float *lpart,
                              cudaStream_t stream, unsigned int *status)
 {
     cudaError_t err;
-    switch (p.d) {
-    case 32: err = launch_d<32, true, BF16>(p, n_splits, opart, lpart, stream, status); break;
-    case 64: err = launch_d<64, true, BF16>(p, n_splits, opart, lpart, stream, status); break;
-    case 128: err = launch_d<128, true, BF16>(p, n_splits, opart, lpart, stream, status); break;
-    default: return cudaErrorInvalidValue;
-    }
-    if (err != cudaSuccess)
-        return err;
-    switch (p.d) {
-    case 32: return launch_merge<32, BF16>(p, n_splits, opart, lpart, stream);
-    case 64: return launch_merge<64, BF16>(p, n_splits, opart, lpart, stream);
-    default: return launch_merge<128, BF16>(p, n_splits, opart, lpart, stream);
+    if constexpr (KIND == kKindTF32) {
+        if (p.d != 32)
+            return cudaErrorInvalidValue;
+        err = launch_d<32, true, KIND>(p, n_splits, opart, lpart, stream, status);
+        if (err != cudaSuccess)
+            return err;
+        return launch_merge<32, KIND>(p, n_splits, opart, lpart, stream);
+    } else {
+        switch (p.d) {
+        case 32: err = launch_d<32, true, KIND>(p, n_splits, opart, lpart, stream, status); break;
+        case 64: err = launch_d<64, true, KIND>(p, n_splits, opart, lpart, stream, status); break;
+        case 128: err = launch_d<128, true, KIND>(p, n_splits, opart, lpart, stream, status); break;
+        default: return cudaErrorInvalidValue;
+        }
+        if (err != cudaSuccess)
+            return err;
+        switch (p.d) {
+        case 32: return launch_merge<32, KIND>(p, n_splits, opart, lpart, stream);
+        case 64: return launch_merge<64, KIND>(p, n_splits, opart, lpart, stream);
+        default: return launch_merge<128, KIND>(p, n_splits, opart, lpart, stream);
+        }
     }
 }
 
@@ -1236,8 +1465,9 @@ cudaError_t launch_splitkv_t(const FwdParams &p, int n_splits, float *opart, flo
 cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
     switch (p.dtype) {
-    case kDtypeF16: return launch_tcgen05_t<false>(p, stream, status);
-    case kDtypeBF16: return launch_tcgen05_t<true>(p, stream, status);
+    case kDtypeF16: return launch_tcgen05_t<kKindF16>(p, stream, status);
+    case kDtypeBF16: return launch_tcgen05_t<kKindBF16>(p, stream, status);
+    case kDtypeF32: return launch_tcgen05_t<kKindTF32>(p, stream, status);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1246,8 +1476,9 @@ cudaError_t launch_tcgen05_splitkv(const FwdParams &p, int n_splits, float *opar
                                    cudaStream_t stream, unsigned int *status)
 {
     switch (p.dtype) {
-    case kDtypeF16: return launch_splitkv_t<false>(p, n_splits, opart, lpart, stream, status);
-    case kDtypeBF16: return launch_splitkv_t<true>(p, n_splits, opart, lpart, stream, status);
+    case kDtypeF16: return launch_splitkv_t<kKindF16>(p, n_splits, opart, lpart, stream, status);
+    case kDtypeBF16: return launch_splitkv_t<kKindBF16>(p, n_splits, opart, lpart, stream, status);
+    case kDtypeF32: return launch_splitkv_t<kKindTF32>(p, n_splits, opart, lpart, stream, status);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -11,7 +11,7 @@ Recipe (one numpy PCG64 stream per workload, seeded with the workload's seed):
   key_lengths[b] ~ uniform integer in [lo, hi] (inclusive). Cross-attention and
   grouped-query workloads draw Q as [B, H, N, d] and K, V as [B, H_kv, N_k, d] in the
   same order. bf16 workloads round the same float32 draws to bfloat16 (nearest even)
-  and hold them as uint16 bit patterns.
+  and hold them as uint16 bit patterns; fp32 workloads keep the float32 draws.
 
 The shapes are the workloads the method is measured on: a tiny exact check, a
 cross-encoder reranking batch (the "cuda-reranker" README's shape class: many
@@ -45,7 +45,7 @@ class Workload:
     ignore_padded_queries: bool = False
     Hkv: int | None = None  # key/value heads (None: H, multi-head attention)
     Nk: int | None = None   # keys per head (None: N, self-attention)
-    dtype: str = "f16"      # "f16" or "bf16" (uint16 bit patterns)
+    dtype: str = "f16"      # "f16", "bf16" (uint16 bit patterns) or "f32"
 
     @property
     def H_kv(self) -> int:
@@ -89,6 +89,9 @@ WORKLOADS = {
     "chunk_prefill": Workload("chunk_prefill", 2, 32, 1024, 128, True, seed=8, Hkv=8, Nk=16384),
     # the prefill shape with bf16 inputs
     "prefill_bf16": Workload("prefill_bf16", 4, 32, 4096, 128, True, seed=9, dtype="bf16"),
+    # the reranking shape with fp32 inputs (the precision of the reranker's own kernel)
+    "rerank_f32": Workload("rerank_f32", 50, 12, 256, 32, False, seed=10, key_len_range=(64, 256),
+                           ignore_padded_queries=True, dtype="f32"),
 }
 
 
@@ -124,17 +127,19 @@ def draw(B: int, H: int, N: int, d: int, seed: int, *, sigma_qk: float = 1.0,
 def draw_ex(B: int, H: int, Hkv: int, N: int, Nk: int, d: int, seed: int, *,
             sigma_qk: float = 1.0, sigma_v: float = 1.0,
             key_len_range: tuple[int, int] | None = None, dtype: str = "f16"):
-    """Returns (q, k, v, key_lengths): q [B,H,N,d], k and v [B,Hkv,Nk,d] (fp16, or uint16
-    bfloat16 bit patterns for dtype "bf16"), key_lengths int32 [B] or None. With Hkv = H,
-    Nk = N and fp16 the draws are those of draw()."""
-    if dtype not in ("f16", "bf16"):
-        raise ValueError("dtype must be 'f16' or 'bf16'")
+    """Returns (q, k, v, key_lengths): q [B,H,N,d], k and v [B,Hkv,Nk,d] (fp16, uint16
+    bfloat16 bit patterns for dtype "bf16", or float32 for "f32"), key_lengths int32 [B] or
+    None. With Hkv = H, Nk = N and fp16 the draws are those of draw()."""
+    if dtype not in ("f16", "bf16", "f32"):
+        raise ValueError("dtype must be 'f16', 'bf16' or 'f32'")
     rng = np.random.Generator(np.random.PCG64(seed))
 
     def normal(shape, sigma):
         x = rng.standard_normal(shape, dtype=np.float32)
         if sigma != 1.0:
             x *= np.float32(sigma)
+        if dtype == "f32":
+            return x
         return x.astype(np.float16) if dtype == "f16" else to_bf16_bits(x)
 
     q = normal((B, H, N, d), sigma_qk)

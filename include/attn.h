@@ -66,10 +66,15 @@ typedef enum {
 
 /* Element type of Q, K, V and O for attn_fwd_ex / attn_fwd_splitkv_ex (the other entry points
  * take fp16). bf16 (8-bit exponent, 8-bit significand) runs on the tiled tcgen05 kernel only,
- * with P rounded to bf16 as well: one tcgen05 MMA takes A and B of the same type. */
+ * with P rounded to bf16 as well: one tcgen05 MMA takes A and B of the same type. fp32
+ * (the "cuda-reranker" README's precision, on the tensor cores that README names as its next
+ * step) takes fp32 Q, K, V and writes fp32 O, d = 32 only, on the tcgen05 kernel: both
+ * products run as TF32 (the tensor core uses the sign, the exponent and the 10 leading fraction
+ * bits of each fp32 operand, P included), accumulation and the softmax statistics are fp32. */
 typedef enum {
     ATTN_DTYPE_F16 = 0,
-    ATTN_DTYPE_BF16 = 1
+    ATTN_DTYPE_BF16 = 1,
+    ATTN_DTYPE_F32 = 2
 } attn_dtype_t;
 
 /* Which kernel runs the forward. AUTO runs the short-sequence kernel for d = 32 with
@@ -143,7 +148,8 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
  *                N_k - N_q earlier tokens). The pages fix no alignment for N_q != N_k; this is
  *                the reading taken. Rows with no allowed key get O = 0 and lse = -inf.
  *   dtype        attn_dtype_t of q, k, v and o (all four the same): ATTN_DTYPE_F16, or
- *                ATTN_DTYPE_BF16 (tcgen05 kernel only); another value is ATTN_ERR_UNSUPPORTED
+ *                ATTN_DTYPE_BF16 (tcgen05 kernel only), or ATTN_DTYPE_F32 (tcgen05 kernel,
+ *                d = 32 only); another value or d is ATTN_ERR_UNSUPPORTED
  *   path         ATTN_PATH_AUTO (for fp16 self-attention shapes the kernel attn_auto_path
  *                selects, the tcgen05 kernel otherwise), ATTN_PATH_TCGEN05 or
  *                ATTN_PATH_WARP_MMA (fp16); ATTN_PATH_SHORT takes fp16 self-attention shapes

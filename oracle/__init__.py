@@ -74,7 +74,7 @@ class Oracle:
         """Oracle forward.
 
         dtype "f16": q, k, v are numpy float16 arrays; "bf16": numpy uint16 (or int16) arrays
-        of bfloat16 bit patterns.
+        of bfloat16 bit patterns; "f32": numpy float32 arrays.
         q: [B, H, N, d] (N query rows per head); k, v: [B, Hkv, Nk, d]
         with H a multiple of Hkv (query head h reads key/value head h // (H // Hkv)).
         Self-attention is k, v of q's shape. With causal and Nk != N, query i sees
@@ -93,8 +93,11 @@ class Oracle:
                 if np.asarray(x).dtype not in (np.uint16, np.int16):
                     raise TypeError("bf16 inputs are uint16/int16 arrays of bit patterns")
             q, k, v = (np.ascontiguousarray(x).view(np.uint16) for x in (q, k, v))
+        elif dtype == "f32":
+            code = 2
+            q, k, v = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v))
         else:
-            raise ValueError("dtype must be 'f16' or 'bf16'")
+            raise ValueError("dtype must be 'f16', 'bf16' or 'f32'")
         if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape:
             raise ValueError("q must be [B,H,N,d] and k, v one [B,Hkv,Nk,d] shape")
         B, H, N, d = q.shape

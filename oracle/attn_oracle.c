@@ -6,8 +6,8 @@
  * and its Python binding) never calls it, and this file includes nothing from
  * the product path.
  *
- * What it computes, for every batch b, query head h and query row i (inputs fp16 or
- * bf16, d innermost; Q and O [B,H,Nq,d], K and V [B,Hkv,Nk,d]; query head h reads key/value
+ * What it computes, for every batch b, query head h and query row i (inputs fp16,
+ * bf16 or fp32, d innermost; Q and O [B,H,Nq,d], K and V [B,Hkv,Nk,d]; query head h reads key/value
  * head h / (H / Hkv), grouped-query attention, Hkv = H being multi-head attention;
  * self-attention is Nq = Nk = N):
  *
@@ -46,8 +46,8 @@
  *
  * The score row is held explicitly (one row of S at a time, never the N x N
  * matrix) and the softmax is the two-pass definition. Inputs are decoded from
- * IEEE-754 binary16 (or bfloat16) to double exactly, so input rounding is not an
- * error source.
+ * IEEE-754 binary16 (or bfloat16, or binary32) to double exactly, so input rounding
+ * is not an error source.
  * Work is split across POSIX threads over (batch*head, block of query rows).
  */
 #include <math.h>
@@ -153,7 +153,8 @@ static void attention_row(const double *q, const double *K, const double *V, int
 }
 
 typedef struct {
-    const uint16_t *q, *k, *v;
+    const void *q, *k, *v;
+    int dtype;          /* 0: binary16, 1: bfloat16 (16-bit patterns), 2: binary32 */
     int64_t B, H, N, d; /* N: query rows per head */
     int64_t Hkv, Nk;    /* key/value heads per batch, keys per head */
     const double *dec;  /* decode table of the input format (fp16 or bf16) */
@@ -172,6 +173,17 @@ typedef struct {
 } job_t;
 
 static int64_t row_id(const job_t *J, int64_t t) { return J->rows ? J->rows[t] : t; }
+
+/* Element idx of an input tensor, decoded exactly to double. */
+static double load_elem(const job_t *J, const void *base, int64_t idx)
+{
+    if (J->dtype == 2) {
+        float f;
+        memcpy(&f, (const unsigned char *)base + idx * 4, sizeof f);
+        return (double)f;
+    }
+    return J->dec[((const uint16_t *)base)[idx]];
+}
 
 static void *worker(void *arg)
 {
@@ -202,16 +214,14 @@ static void *worker(void *arg)
             int64_t bh = r / N, i = r % N, b = bh / J->H, h = bh % J->H;
             int64_t kvh = b * J->Hkv + h / G; /* the key/value head query head h reads */
             if (kvh != decoded_head) {
-                const uint16_t *kh = J->k + kvh * Nk * d, *vh = J->v + kvh * Nk * d;
                 for (int64_t e = 0; e < Nk * d; ++e) {
-                    K[e] = J->dec[kh[e]];
-                    V[e] = J->dec[vh[e]];
+                    K[e] = load_elem(J, J->k, kvh * Nk * d + e);
+                    V[e] = load_elem(J, J->v, kvh * Nk * d + e);
                 }
                 decoded_head = kvh;
             }
-            const uint16_t *qr = J->q + r * d;
             for (int64_t c = 0; c < d; ++c)
-                q[c] = J->dec[qr[c]];
+                q[c] = load_elem(J, J->q, r * d + c);
             int64_t L = Nk;
             if (J->key_lengths) {
                 L = J->key_lengths[b];
@@ -231,20 +241,20 @@ static void *worker(void *arg)
 
 /*
  * Computes O (and lse) for the listed query rows, or for all B*H*Nq rows when
- * rows == NULL. q: 16-bit float bit patterns [B,H,Nq,d]; k, v: [B,Hkv,Nk,d], H a
- * multiple of Hkv; dtype 0: IEEE binary16, 1: bfloat16. key_lengths: [B] or NULL. rows: flat row ids (b*H + h)*Nq + i in
+ * rows == NULL. q: [B,H,Nq,d]; k, v: [B,Hkv,Nk,d], H a multiple of Hkv; elements
+ * are dtype 0: IEEE binary16, 1: bfloat16 (16-bit patterns), 2: IEEE binary32. key_lengths: [B] or NULL. rows: flat row ids (b*H + h)*Nq + i in
  * ascending order, n_rows of them. o: [n_rows, d] doubles (or [B,H,Nq,d] when
  * rows == NULL); lse: [n_rows] or NULL. n_threads <= 0 uses one thread. Returns 0
  * on success, -1 on bad arguments, -2 when memory runs out.
  */
-int oracle_attn_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B, int64_t H,
+int oracle_attn_ex(const void *q, const void *k, const void *v, int64_t B, int64_t H,
                    int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int dtype, double sm_scale,
                    int causal, const int32_t *key_lengths, const int64_t *rows, int64_t n_rows,
                    double *o, double *lse, int n_threads)
 {
     const int64_t N = Nq;
     if (!q || !k || !v || !o || B < 0 || H < 0 || N < 0 || Nk < 0 || d <= 0 || Hkv < 1 ||
-        H % Hkv != 0 || (dtype != 0 && dtype != 1))
+        H % Hkv != 0 || dtype < 0 || dtype > 2)
         return -1;
     int64_t total = B * H * N;
     if (!rows)
@@ -280,6 +290,7 @@ int oracle_attn_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
     J.q = q; J.k = k; J.v = v;
     J.B = B; J.H = H; J.N = N; J.d = d;
     J.Hkv = Hkv; J.Nk = Nk;
+    J.dtype = dtype;
     J.dec = dtype == 1 ? g_bf16_table : g_half_table;
     J.sm_scale = sm_scale;
     J.causal = causal;

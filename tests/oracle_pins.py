@@ -10,6 +10,7 @@ What pins what:
   numpy's own binary16 -> float64 conversion             -> the fp16 decoder
   numpy's float32 bit view (bfloat16 = upper half)        -> the bf16 decoder
   values exact in both formats (fp16 vs bf16 result)      -> bf16 routing
+  fp16 values as fp32; scipy on full fp32 inputs          -> fp32 inputs
   scipy.special.softmax / logsumexp on tiny inputs       -> scores, masks, softmax, PV, lse
   P1's two-block online-softmax merge                     -> normalisation and lse
   closed forms (uniform keys, one-hot selection, causal
@@ -430,6 +431,28 @@ def pin_bf16_agrees_with_f16_on_common_values(orc):
     assert np.allclose(o, 2.0, atol=1e-12, rtol=0) and np.allclose(lse, 1.0 + math.log(2.0))
 
 
+def pin_f32_inputs(orc):
+    """fp32 inputs: fp16 values (exact in fp32) give the fp16 result's bits; full-precision fp32
+    values match scipy's softmax / logsumexp over the float64 conversion of the same inputs."""
+    B, H, N, d = 2, 2, 11, 6
+    q, k, v = _rand((B, H, N, d), 241), _rand((B, H, N, d), 242), _rand((B, H, N, d), 243)
+    kl = np.array([11, 4], np.int32)
+    for causal in (False, True):
+        o16, l16 = orc.attn(q, k, v, sm_scale=0.4, causal=causal, key_lengths=kl)
+        o32, l32 = orc.attn(q.astype(np.float32), k.astype(np.float32), v.astype(np.float32),
+                            sm_scale=0.4, causal=causal, key_lengths=kl, dtype="f32")
+        assert np.array_equal(o16, o32) and np.array_equal(l16, l32)
+    rng = np.random.Generator(np.random.PCG64(244))
+    qf, kf, vf = (rng.standard_normal((B, H, N, d)).astype(np.float32) for _ in range(3))
+    for causal in (False, True):
+        o, lse = orc.attn(qf, kf, vf, sm_scale=0.4, causal=causal, key_lengths=kl, dtype="f32")
+        ro, rl = _scipy_reference(qf, kf, vf, 0.4, causal, kl)
+        assert np.max(np.abs(o - ro)) < 1e-12
+        fin = np.isfinite(rl)
+        assert np.array_equal(np.isfinite(lse), fin)
+        assert np.max(np.abs(lse[fin] - rl[fin])) < 1e-12
+
+
 ALL_PINS = [
     pin_half_decoder,
     pin_dot_product_golden,
@@ -451,4 +474,5 @@ ALL_PINS = [
     pin_cross_gqa_uniform_keys,
     pin_bf16_decoder,
     pin_bf16_agrees_with_f16_on_common_values,
+    pin_f32_inputs,
 ]

@@ -31,6 +31,9 @@ MUTANTS = {
                            "mag = ldexp((double)(128 + f), e - 133);"),
     "bf16_subnormal_scale": ("mag = ldexp((double)f, -133);", "mag = ldexp((double)f, -134);"),
     "bf16_read_as_f16": ("J.dec = dtype == 1 ? g_bf16_table : g_half_table;", "J.dec = g_half_table;"),
+    "f32_read_as_16bit": ("if (J->dtype == 2) {", "if (J->dtype == 3) {"),
+    "f32_wrong_stride": ("memcpy(&f, (const unsigned char *)base + idx * 4, sizeof f);",
+                         "memcpy(&f, (const unsigned char *)base + idx * 2, sizeof f);"),
 }
 
 

@@ -24,7 +24,7 @@ def run_splitkv(q, k, v, *, causal, key_lengths=None, sm_scale=None, n_splits=0,
     kld = to_dev(key_lengths)
     pad_o, pad_l = 4096, 1024
     n_o, n_l = q.size, B * H * N
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32}.get(dtype, torch.float16)
     o_buf = torch.full((n_o + 2 * pad_o,), float("nan"), dtype=tdt, device="cuda")
     l_buf = torch.full((n_l + 2 * pad_l,), float("nan"), dtype=torch.float32, device="cuda")
     o_buf[:pad_o] = 1234.0
