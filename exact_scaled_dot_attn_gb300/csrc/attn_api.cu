@@ -107,9 +107,27 @@ attn::FwdParams make_params(const void *q, const void *k, const void *v, void *o
 
 Shape self_shape(int B, int H, int N, int d) { return Shape{B, H, H, N, N, d, ATTN_DTYPE_F16}; }
 
+// Grouped-query attention with few query rows: the G = H / H_kv query heads that share a
+// key/value head are adjacent in Q, O and lse ([B, H, N_q, d] = [B, H_kv, G * N_q, d]), so the
+// problem is the same attention with H_kv heads of G * N_q query rows each, and the rows of a
+// group fill one Q tile together. Exact whenever every packed row keeps its allowed keys:
+// without the causal mask, or with it and one query row (query 0 sees keys j <= N_k - 1, i.e.
+// every key). Applied below 128 query rows, where a head alone would leave a tile mostly empty.
+void pack_query_groups(Shape &sh, int &causal)
+{
+    if (sh.Hkv < sh.H && sh.Nq < 128 && (!causal || sh.Nq == 1)) {
+        const long long rows = static_cast<long long>(sh.H / sh.Hkv) * sh.Nq;
+        if (rows <= INT32_MAX) {
+            sh.Nq = static_cast<int>(rows);
+            sh.H = sh.Hkv;
+            causal = 0;
+        }
+    }
+}
+
 // One forward pass on the chosen kernel (the automatic choice when path is ATTN_PATH_AUTO).
-attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh,
-                      float sm_scale, int causal, const int32_t *key_lengths, int path,
+attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh_in,
+                      float sm_scale, int causal_in, const int32_t *key_lengths, int path,
                       const attn_debug_opts_t *opts, attn_stream_t stream);
 
 } // namespace
@@ -141,16 +159,22 @@ extern "C" int attn_auto_path(int N, int d)
 
 namespace {
 
-attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh,
-                      float sm_scale, int causal, const int32_t *key_lengths, int path,
+attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh_in,
+                      float sm_scale, int causal_in, const int32_t *key_lengths, int path,
                       const attn_debug_opts_t *opts, attn_stream_t stream)
 {
-    attn_status_t st = validate(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
+    attn_status_t st = validate(q, k, v, o, lse, sh_in, sm_scale, causal_in, key_lengths);
     if (st != ATTN_OK)
         return st;
     if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
         path != ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
+    // an explicitly chosen short-sequence kernel takes only the shapes the caller gave it
+    if (path == ATTN_PATH_SHORT && !sh_in.self())
+        return ATTN_ERR_UNSUPPORTED;
+    Shape sh = sh_in;
+    int causal = causal_in;
+    pack_query_groups(sh, causal);
     // The short-sequence kernel serves fp16 self-attention only; bf16 and fp32 run on the
     // tiled tcgen05 kernel only.
     if (path == ATTN_PATH_SHORT && (!sh.self() || sh.Nq > 256 || sh.d > 64))
@@ -305,12 +329,14 @@ extern "C" attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const
                                              const int32_t *key_lengths, int n_splits, void *workspace,
                                              size_t workspace_bytes, attn_stream_t stream)
 {
-    const Shape sh{B, H, H_kv, N_q, N_k, d, dtype};
+    Shape sh{B, H, H_kv, N_q, N_k, d, dtype};
     attn_status_t st = validate(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
         return st;
+    // (the workspace holds one partial row per query row: B * H * N_q either way)
+    pack_query_groups(sh, causal);
     if (n_splits <= 0) {
-        n_splits = attn_splitkv_auto_splits_ex(B, H, N_q, N_k, d, causal);
+        n_splits = attn_splitkv_auto_splits_ex(sh.B, sh.H, sh.Nq, sh.Nk, d, causal);
         if (n_splits < 1)
             return ATTN_ERR_INVALID_ARG;
     }

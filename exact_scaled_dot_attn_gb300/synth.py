@@ -87,6 +87,9 @@ WORKLOADS = {
     # a block of 1024 new queries over a cached context of 16384 keys (cross-attention shape,
     # causal diagonal at the last rows), grouped-query heads
     "chunk_prefill": Workload("chunk_prefill", 2, 32, 1024, 128, True, seed=8, Hkv=8, Nk=16384),
+    # decoding one token per sequence over a cache of 8192 keys, 32 query heads over 8 key/value
+    # heads (the diagonal of the causal mask leaves every key to the one query)
+    "decode_gqa": Workload("decode_gqa", 8, 32, 1, 128, True, seed=11, Hkv=8, Nk=8192),
     # the prefill shape with bf16 inputs
     "prefill_bf16": Workload("prefill_bf16", 4, 32, 4096, 128, True, seed=9, dtype="bf16"),
     # the reranking shape with fp32 inputs (the precision of the reranker's own kernel)

@@ -30,6 +30,13 @@ CASES = [
     (2, 2, 1, 513, 257, 32, True, [257, 130]),
     (1, 3, 3, 200, 64, 128, False, None),
     (2, 4, 4, 384, 640, 64, True, [640, 300]),
+    # decode-sized query blocks: the G query heads of a group run as G * N_q packed rows
+    (2, 8, 2, 1, 1000, 128, True, [1000, 37]),
+    (3, 12, 4, 5, 300, 64, False, [300, 1, 0]),
+    (1, 32, 8, 16, 2048, 128, False, None),
+    (2, 4, 1, 1, 64, 32, True, None),
+    (2, 8, 2, 16, 64, 32, False, [64, 20]),   # packed: 64 rows over 64 keys, a self-attention shape
+    (1, 8, 2, 4, 500, 64, True, None),        # causal with N_q > 1: not packed
 ]
 
 
