@@ -547,8 +547,8 @@ def variants(torch, api, peaks, peak_src):
     qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
     od = torch.empty_like(qd)
     nbytes = synth.min_bytes_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d)
-    n_splits = int(api._lib.lib().attn_splitkv_auto_splits_ex(w.B, w.H_kv, (w.H // w.H_kv) * w.N, w.N_k,
-                                                               w.d, 0))
+    n_splits = int(api._lib.lib().attn_splitkv_auto_splits_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d,
+                                                               int(w.causal)))
     ws = torch.empty(api.splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits), dtype=torch.uint8,
                      device="cuda")
 

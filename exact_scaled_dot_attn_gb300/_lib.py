@@ -53,7 +53,7 @@ SIGNATURES = {
     "attn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_splitkv_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i,
                                  _vp, ctypes.c_size_t, _vp]),
-    "attn_splitkv_auto_splits_ex": (_i, [_i, _i, _i, _i, _i, _i]),
+    "attn_splitkv_auto_splits_ex": (_i, [_i, _i, _i, _i, _i, _i, _i]),
 }
 
 _lib = None

@@ -144,7 +144,7 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bo
     L = _lib.lib()
     with torch.cuda.device(dev):
         if n_splits <= 0:
-            n_splits = L.attn_splitkv_auto_splits_ex(B, H, N, Nk, d, int(bool(causal)))
+            n_splits = L.attn_splitkv_auto_splits_ex(B, H, Hkv, N, Nk, d, int(bool(causal)))
         need = L.attn_splitkv_workspace_bytes(B, H, N, d, int(n_splits))
         if need == 0:
             raise ValueError(f"invalid split-KV sizes (n_splits={n_splits})")

@@ -268,17 +268,20 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S)
     return static_cast<size_t>(total);
 }
 
-// Ranges per (batch*head, Q tile pair) for the automatic choice: enough (pair, range) units
-// that the largest one is no longer than an SM's average share. Without a causal mask every
-// pair has the same work and one unit per SM suffices; with it the largest pair has
-// (max / mean) of the pairs' K/V tile counts times the average (about 2 for self-attention).
-// At most one range per two K/V tiles, at most kMaxSplits.
+// Ranges per (batch*head, Q tile pair) for the automatic choice. Without the causal mask every
+// (pair, range) unit has the same length, so the most ranges that still give one unit per SM
+// (floor(SMs / pairs)) shorten the launch without adding a second wave. With it, enough units
+// that the largest is no longer than an SM's average share: the largest pair's K/V tile count
+// over the mean (about 2 for self-attention; from the shifted diagonal for cross-attention)
+// times SMs / pairs, rounded up. At most one range per two K/V tiles, at most kMaxSplits.
 int auto_splits(int B, int H, int Nq, int Nk, int causal, int sms)
 {
     const int n_pairs = (Nq + 255) / 256;
     const long long pairs = static_cast<long long>(B) * H * n_pairs;
-    double skew = 1.0;
-    if (causal) {
+    long long want;
+    if (!causal) {
+        want = sms / pairs;
+    } else {
         long long sum = 0, mx = 0;
         for (int pr = 0; pr < n_pairs; ++pr) {
             long long e = static_cast<long long>(pr) * 256 + 256 + Nk - Nq;
@@ -287,10 +290,9 @@ int auto_splits(int B, int H, int Nq, int Nk, int causal, int sms)
             sum += f;
             mx = f > mx ? f : mx;
         }
-        if (sum > 0)
-            skew = static_cast<double>(mx) * n_pairs / static_cast<double>(sum);
+        const double skew = sum > 0 ? static_cast<double>(mx) * n_pairs / static_cast<double>(sum) : 1.0;
+        want = static_cast<long long>(std::ceil(static_cast<double>(sms) * skew / pairs));
     }
-    const long long want = static_cast<long long>(std::ceil(static_cast<double>(sms) * skew / pairs));
     const int kv_tiles = (Nk + 127) / 128;
     long long s = want < 1 ? 1 : want;
     if (s > kv_tiles / 2)
@@ -307,20 +309,23 @@ extern "C" size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n
     return splitkv_bytes(B, H, N, d, n_splits);
 }
 
-extern "C" int attn_splitkv_auto_splits_ex(int B, int H, int N_q, int N_k, int d, int causal)
+extern "C" int attn_splitkv_auto_splits_ex(int B, int H, int H_kv, int N_q, int N_k, int d, int causal)
 {
-    if (B < 1 || H < 1 || N_q < 1 || N_k < 1 || (d != 32 && d != 64 && d != 128) ||
-        (causal != 0 && causal != 1))
+    if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_k < 1 ||
+        (d != 32 && d != 64 && d != 128) || (causal != 0 && causal != 1))
         return -1;
     int sms = 0;
     if (attn::device_sm_count(&sms) != cudaSuccess || sms < 1)
         sms = 148;
-    return auto_splits(B, H, N_q, N_k, causal, sms);
+    // the shape the kernels run (query heads of a group packed together, see pack_query_groups)
+    Shape sh{B, H, H_kv, N_q, N_k, d, ATTN_DTYPE_F16};
+    pack_query_groups(sh, causal);
+    return auto_splits(sh.B, sh.H, sh.Nq, sh.Nk, causal, sms);
 }
 
 extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal)
 {
-    return attn_splitkv_auto_splits_ex(B, H, N, N, d, causal);
+    return attn_splitkv_auto_splits_ex(B, H, H, N, N, d, causal);
 }
 
 extern "C" attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, void *o,
@@ -333,13 +338,13 @@ extern "C" attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const
     attn_status_t st = validate(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (st != ATTN_OK)
         return st;
-    // (the workspace holds one partial row per query row: B * H * N_q either way)
-    pack_query_groups(sh, causal);
     if (n_splits <= 0) {
-        n_splits = attn_splitkv_auto_splits_ex(sh.B, sh.H, sh.Nq, sh.Nk, d, causal);
+        n_splits = attn_splitkv_auto_splits_ex(B, H, H_kv, N_q, N_k, d, causal);
         if (n_splits < 1)
             return ATTN_ERR_INVALID_ARG;
     }
+    // (the workspace holds one partial row per query row: B * H * N_q either way)
+    pack_query_groups(sh, causal);
     if (n_splits > kMaxSplits)
         return ATTN_ERR_INVALID_ARG;
     const size_t need = splitkv_bytes(B, H, N_q, d, n_splits);

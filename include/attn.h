@@ -192,17 +192,19 @@ attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void
  * outputs and logsumexps of every range). 0 for invalid sizes or n_splits outside 1..16. */
 size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 
-/* The split count attn_fwd_splitkv uses for n_splits <= 0: enough (Q tile pair, key range)
- * units that the largest is no longer than an SM's average share on the current device (one
- * unit per SM without a causal mask; with it the largest pair's K/V tile count over the mean,
- * about two), at most one range per two 128-key tiles and at most 16. -1 for invalid sizes. */
+/* The split count attn_fwd_splitkv uses for n_splits <= 0, for the current device's SM count:
+ * without a causal mask the most ranges that still give one (Q tile pair, key range) unit per
+ * SM (SMs / pairs, rounded down); with it enough units that the largest is no longer than an
+ * SM's average share (the largest pair's K/V tile count over the mean, about two, times SMs /
+ * pairs, rounded up). At most one range per two 128-key tiles and at most 16; at least 1. -1
+ * for invalid sizes. */
 int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
 /* Split-KV forward of cross-attention and grouped-query attention: the result of attn_fwd_ex
  * (shapes, head groups, causal alignment and dtype as there), computed as attn_fwd_splitkv
  * computes it.
  * The workspace is sized by attn_splitkv_workspace_bytes(B, H, N_q, d, n_splits) (query rows);
- * n_splits <= 0 takes attn_splitkv_auto_splits_ex(B, H, N_q, N_k, d, causal). With H_kv = H and
+ * n_splits <= 0 takes attn_splitkv_auto_splits_ex(B, H, H_kv, N_q, N_k, d, causal). With H_kv = H and
  * N_q = N_k and fp16 it is attn_fwd_splitkv. */
 attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                                   int B, int H, int H_kv, int N_q, int N_k, int d, int dtype,
@@ -210,10 +212,12 @@ attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, v
                                   int n_splits, void *workspace, size_t workspace_bytes,
                                   attn_stream_t stream);
 
-/* attn_splitkv_auto_splits for N_q query rows over N_k keys: under the causal mask the largest
- * pair's work over the mean is taken from the pairs' 128-key tile counts with the diagonal of
- * attn_fwd_ex. -1 for invalid sizes. */
-int attn_splitkv_auto_splits_ex(int B, int H, int N_q, int N_k, int d, int causal);
+/* attn_splitkv_auto_splits for the shapes of attn_fwd_ex (H query heads over H_kv key/value heads,
+ * N_q query rows over N_k keys), counted on the problem the kernels run (query heads of a group
+ * packed together where attn_fwd_ex packs them); under the causal mask the largest pair's work
+ * over the mean is taken from the pairs' 128-key tile counts with the diagonal of attn_fwd_ex.
+ * -1 for invalid sizes. */
+int attn_splitkv_auto_splits_ex(int B, int H, int H_kv, int N_q, int N_k, int d, int causal);
 
 /*
  * Split-KV forward that allocates nothing (the pages have no counterpart: this is a service of

@@ -175,6 +175,7 @@ def test_splitkv_ex_validation(lib):
     assert lib.attn_fwd_splitkv_ex(*bad, 2, A, 1 << 30, None) == _lib.ATTN_ERR_INVALID_ARG
     bad_dtype = (A, A, A, A, None, 1, 4, 2, 8, 32, 64, 5, 0.125, 0, None)
     assert lib.attn_fwd_splitkv_ex(*bad_dtype, 2, A, 1 << 30, None) == _lib.ATTN_ERR_UNSUPPORTED
-    assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 0, 64, 0) == -1
-    assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 32, 48, 0) == -1
-    assert lib.attn_splitkv_auto_splits_ex(1, 4, 8, 32, 64, 2) == -1
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 2, 8, 0, 64, 0) == -1
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 2, 8, 32, 48, 0) == -1
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 2, 8, 32, 64, 2) == -1
+    assert lib.attn_splitkv_auto_splits_ex(1, 4, 3, 8, 32, 64, 0) == -1  # H not a multiple of H_kv
