@@ -43,8 +43,9 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Sizes of one call: H query heads of N_q rows, H_kv key/value heads of N_k keys.
 struct Shape {
     int B, H, Hkv, Nq, Nk, d;
-    int dtype; // attn_dtype_t
-    bool self() const { return Hkv == H && Nq == Nk; }
+    int dtype;     // attn_dtype_t
+    int qrows = 0; // packed query groups under the causal mask: query rows of one head
+    bool self() const { return Hkv == H && Nq == Nk && qrows == 0; }
 };
 
 attn_status_t validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -94,6 +95,7 @@ attn::FwdParams make_params(const void *q, const void *k, const void *v, void *o
     p.d = sh.d;
     p.Hkv = sh.Hkv;
     p.Nk = sh.Nk;
+    p.qrows = sh.qrows;
     p.dtype = sh.dtype == ATTN_DTYPE_BF16 ? attn::kDtypeBF16
               : sh.dtype == ATTN_DTYPE_F32 ? attn::kDtypeF32
                                            : attn::kDtypeF16;
@@ -110,17 +112,21 @@ Shape self_shape(int B, int H, int N, int d) { return Shape{B, H, H, N, N, d, AT
 // Grouped-query attention with few query rows: the G = H / H_kv query heads that share a
 // key/value head are adjacent in Q, O and lse ([B, H, N_q, d] = [B, H_kv, G * N_q, d]), so the
 // problem is the same attention with H_kv heads of G * N_q query rows each, and the rows of a
-// group fill one Q tile together. Exact whenever every packed row keeps its allowed keys:
-// without the causal mask, or with it and one query row (query 0 sees keys j <= N_k - 1, i.e.
-// every key). Applied below 128 query rows, where a head alone would leave a tile mostly empty.
+// group fill one Q tile together. Without the causal mask every row keeps its keys; with it
+// and one query row, query 0 sees every key (j <= N_k - 1), so the mask goes; with it and more
+// rows, the kernels take row r as query r % N_q (qrows). Applied below 128 query rows, where a
+// head alone would leave a tile mostly empty.
 void pack_query_groups(Shape &sh, int &causal)
 {
-    if (sh.Hkv < sh.H && sh.Nq < 128 && (!causal || sh.Nq == 1)) {
+    if (sh.Hkv < sh.H && sh.Nq < 128) {
         const long long rows = static_cast<long long>(sh.H / sh.Hkv) * sh.Nq;
         if (rows <= INT32_MAX) {
+            if (causal && sh.Nq > 1)
+                sh.qrows = sh.Nq;
+            else
+                causal = 0;
             sh.Nq = static_cast<int>(rows);
             sh.H = sh.Hkv;
-            causal = 0;
         }
     }
 }
@@ -320,7 +326,8 @@ extern "C" int attn_splitkv_auto_splits_ex(int B, int H, int H_kv, int N_q, int 
     // the shape the kernels run (query heads of a group packed together, see pack_query_groups)
     Shape sh{B, H, H_kv, N_q, N_k, d, ATTN_DTYPE_F16};
     pack_query_groups(sh, causal);
-    return auto_splits(sh.B, sh.H, sh.Nq, sh.Nk, causal, sms);
+    // packed groups under the causal mask: every pair sees all keys, as without the mask
+    return auto_splits(sh.B, sh.H, sh.Nq, sh.Nk, sh.qrows ? 0 : causal, sms);
 }
 
 extern "C" int attn_splitkv_auto_splits(int B, int H, int N, int d, int causal)

@@ -25,6 +25,9 @@ struct FwdParams {
     int Hkv, Nk;    // key/value heads per batch (H a multiple of Hkv) and keys per head;
                     // self-attention: Hkv = H, Nk = N. Query head h reads key/value head
                     // h / (H / Hkv); under the causal mask query i sees keys j <= i + Nk - N.
+    int qrows;      // 0, or the query rows of one head when the rows of several query heads are
+                    // packed into one problem (N = G * qrows, qrows < 128): under the causal
+                    // mask row r is query r % qrows and sees keys j <= r % qrows + Nk - qrows.
     float sm_scale;
     float scale_log2; // sm_scale * log2(e): scores are exponentiated with exp2
     int causal;

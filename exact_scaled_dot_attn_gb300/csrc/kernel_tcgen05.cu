@@ -211,7 +211,9 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
     }
     U.L = L;
     int kv_end0 = L, kv_end1 = L;
-    if (a.p.causal) {
+    // (packed query groups: every 128-row tile holds a last query of some head, so no K/V
+    // tile is skipped by the causal mask)
+    if (a.p.causal && !a.p.qrows) {
         // Q tile 0 stops at its own diagonal (query i sees keys j <= i + Nk - N)
         const int off = a.p.Nk - a.p.N;
         kv_end0 = max(0, min(L, U.q0 + kBM + off));
@@ -952,6 +954,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = lane_base + (t ? C::kTmemS1 : C::kTmemS0);
         const float scale = p.scale_log2;
         const int diag = p.Nk - p.N; // causal: query i sees keys j <= i + diag
+        // packed query groups: row r is query r % qrows, whose diagonal is at Nk - qrows; every
+        // tile holds a query 0, the row that sees the fewest keys
+        const int qdiag = p.qrows ? p.Nk - p.qrows : diag;
         uint32_t s_it = 0;
         uint32_t pv_par = 0; // bit b: parity of the PV products committed into O buffer b
         uint32_t ucnt = 0;   // units in which this tile took part
@@ -1098,10 +1103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++s_it;
                 tc_fence_after();
                 const int kv0 = (U.j0 + j) * kBN;
-                const bool need_mask = (kv0 + kBN > U.L) || (p.causal && kv0 + kBN - 1 > tile_row0 + diag);
+                const bool need_mask = (kv0 + kBN > U.L) ||
+                                       (p.causal && kv0 + kBN - 1 > (p.qrows ? qdiag : tile_row0 + diag));
                 int lim = U.L - kv0; // keys [kv0, kv0 + lim) are allowed for this row
                 if (p.causal)
-                    lim = min(lim, row + diag - kv0 + 1);
+                    lim = min(lim, (p.qrows ? row % p.qrows : row) + qdiag - kv0 + 1);
 
                 uint32_t sv[kBN];
                 tmem_ld128(tS, sv);
@@ -1338,7 +1344,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
         return cudaErrorInvalidConfiguration;
     const int grid = a.n_units < sms ? a.n_units : sms;
     std::shared_ptr<SchedTable> sched =
-        schedule_for(BH, p.N, p.Nk, p.causal, a.head_block, a.n_pairs, n_splits, grid);
+        schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block, a.n_pairs, n_splits, grid);
     kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
     return cudaGetLastError();
 }

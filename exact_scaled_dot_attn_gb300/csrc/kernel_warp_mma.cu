@@ -57,8 +57,10 @@ __global__ void __launch_bounds__(kThreads)
         L = L < 0 ? 0 : (L > Nk ? Nk : L);
     }
     int kv_end = L;
-    if (p.causal)
+    if (p.causal && !p.qrows) // (packed query groups: every tile sees all keys up to L)
         kv_end = max(0, min(kv_end, q0 + kBM + diag));
+    // packed query groups: row r is query r % qrows, whose diagonal is at Nk - qrows
+    const int qdiag = p.qrows ? Nk - p.qrows : diag;
     const int n_tiles = (kv_end + kBN - 1) / kBN;
 
     const size_t head_off = static_cast<size_t>(bh) * N * D;
@@ -106,10 +108,13 @@ __global__ void __launch_bounds__(kThreads)
         if (t == 0)
             w.load_q(sQ, wrow0, lane);
         const int kv0 = t * kBN;
-        const bool need_mask = (kv0 + kBN > L) || (p.causal && kv0 + kBN - 1 > q0 + wrow0 + diag);
+        const bool need_mask = (kv0 + kBN > L) ||
+                               (p.causal && kv0 + kBN - 1 > (p.qrows ? qdiag : q0 + wrow0 + diag));
         // the masks compare keys with the diagonal column of each row: row + diag
-        w.tile(sK + st * kBN * D, sV + st * kBN * D, kv0, L, p.causal != 0, need_mask, row_a + diag,
-               row_b + diag, p.scale_log2, lane);
+        const int da = (p.qrows ? row_a % p.qrows : row_a) + qdiag;
+        const int db = (p.qrows ? row_b % p.qrows : row_b) + qdiag;
+        w.tile(sK + st * kBN * D, sV + st * kBN * D, kv0, L, p.causal != 0, need_mask, da, db,
+               p.scale_log2, lane);
         __syncthreads();
     }
     cp_async_wait<0>();
