@@ -157,9 +157,9 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
  * B, H, H_kv, N_q, N_k >= 1 (else ATTN_ERR_INVALID_ARG, as is H not a multiple of H_kv); the
  * element count of every tensor must fit int64 and B*H int32. The other arguments, layouts
  * and errors are those of attn_fwd_lse. With H_kv = H, N_q = N_k and fp16 it is attn_fwd_path.
- * With H_kv < H and N_q < 128, without the causal mask or with N_q = 1, the G = H / H_kv query
- * heads of a group run as one problem of G * N_q query rows (they are adjacent in q, o and lse),
- * so they share Q tiles; the result is the same.
+ * With H_kv < H and N_q < 128 the G = H / H_kv query heads of a group run as one problem of
+ * G * N_q query rows (they are adjacent in q, o and lse), so they share Q tiles; under the causal
+ * mask each packed row keeps its own query's diagonal. The result is the same.
  */
 attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                           int H, int H_kv, int N_q, int N_k, int d, int dtype, float sm_scale,
