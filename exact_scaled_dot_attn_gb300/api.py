@@ -178,23 +178,94 @@ def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, n_splits: int) -> in
     return int(_lib.lib().attn_splitkv_workspace_bytes(B, H, N, d, n_splits))
 
 
+# Host problems at least this large (Q, K, V and O together) are copied and computed in pieces.
+_HOST_CHUNK_MIN_BYTES = 64 << 20
+_HOST_PIECES = 8
+
+
+def _host_pieces(q, k):
+    """Independent pieces of a host problem, at most _HOST_PIECES: (q index, k/v index, batch
+    index) triples, each a run of batches, or a run of key/value heads (with their query-head
+    groups) of one batch, so that every piece is a contiguous block of q, k, v and o. None when
+    the problem is small or cannot be split."""
+    B, H = q.shape[0], q.shape[1]
+    Hkv = k.shape[1]
+    total = (q.numel() * 2 + k.numel() * 2) * q.element_size()
+    if total < _HOST_CHUNK_MIN_BYTES or B * Hkv < 2:
+        return None
+    if B >= _HOST_PIECES:
+        cut = [B * i // _HOST_PIECES for i in range(_HOST_PIECES + 1)]
+        return [((slice(cut[i], cut[i + 1]),), (slice(cut[i], cut[i + 1]),), slice(cut[i], cut[i + 1]))
+                for i in range(_HOST_PIECES)]
+    g = H // Hkv
+    per = max(1, min(Hkv, _HOST_PIECES // B)) # pieces per batch
+    cut = [Hkv * i // per for i in range(per + 1)]
+    return [((slice(b, b + 1), slice(cut[i] * g, cut[i + 1] * g)), (slice(b, b + 1), slice(cut[i], cut[i + 1])),
+             slice(b, b + 1)) for b in range(B) for i in range(per)]
+
+
+_host_streams = {}
+
+
+def _pipeline_streams(dev):
+    """(input copies, kernels, output copies) streams of a device, created once."""
+    key = dev.index
+    if key not in _host_streams:
+        _host_streams[key] = tuple(torch.cuda.Stream(dev) for _ in range(3))
+    return _host_streams[key]
+
+
 def _fwd_host(q, k, v, *, causal, sm_scale, key_lengths, return_lse, out, lse_out, path):
+    """Host tensors in, host tensors out. Large problems go as a pipeline of independent
+    (batch, head) pieces: the input copies run back to back on one stream, each piece's kernel
+    on a second once its inputs are in, and its output copy on a third once it is done, so the
+    copies overlap the kernels and each other. The result is the same as one call."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    qd = q.to(dev, non_blocking=True)
-    kd = k.to(dev, non_blocking=True)
-    vd = v.to(dev, non_blocking=True)
-    kld = key_lengths.to(dev, non_blocking=True) if key_lengths is not None else None
-    res = fwd(qd, kd, vd, causal=causal, sm_scale=sm_scale, key_lengths=kld,
-              return_lse=return_lse, path=path)
-    o_dev, lse_dev = res if return_lse else (res, None)
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-    out.copy_(o_dev, non_blocking=True)
-    if return_lse:
-        if lse_out is None:
-            lse_out = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
-        lse_out.copy_(lse_dev, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
+    if return_lse and lse_out is None:
+        lse_out = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
+    pieces = _host_pieces(q, k)
+    cur = torch.cuda.current_stream(dev)
+    if pieces is None:
+        qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
+        kld = key_lengths.to(dev, non_blocking=True) if key_lengths is not None else None
+        res = fwd(qd, kd, vd, causal=causal, sm_scale=sm_scale, key_lengths=kld,
+                  return_lse=return_lse, path=path)
+        o_dev, lse_dev = res if return_lse else (res, None)
+        out.copy_(o_dev, non_blocking=True)
+        if return_lse:
+            lse_out.copy_(lse_dev, non_blocking=True)
+        cur.synchronize()
+        return (out, lse_out) if return_lse else out
+    s_in, s_run, s_out = _pipeline_streams(dev)
+    for st in (s_in, s_run, s_out):
+        st.wait_stream(cur)
+    keep = []  # device tensors of every piece, alive until the streams are done
+    for qs, ks, bs in pieces:
+        with torch.cuda.stream(s_in):
+            qd = q[qs].to(dev, non_blocking=True)
+            kd = k[ks].to(dev, non_blocking=True)
+            vd = v[ks].to(dev, non_blocking=True)
+            kld = key_lengths[bs].to(dev, non_blocking=True) if key_lengths is not None else None
+            loaded = torch.cuda.Event()
+            loaded.record(s_in)
+        s_run.wait_event(loaded)
+        with torch.cuda.stream(s_run):
+            res = fwd(qd, kd, vd, causal=causal, sm_scale=sm_scale, key_lengths=kld,
+                      return_lse=return_lse, path=path)
+            o_dev, lse_dev = res if return_lse else (res, None)
+            done = torch.cuda.Event()
+            done.record(s_run)
+        s_out.wait_event(done)
+        with torch.cuda.stream(s_out):
+            out[qs].copy_(o_dev, non_blocking=True)
+            if return_lse:
+                lse_out[qs].copy_(lse_dev, non_blocking=True)
+        keep.append((qd, kd, vd, kld, o_dev, lse_dev))
+    s_out.synchronize()
+    for st in (s_in, s_run):
+        st.synchronize()
     return (out, lse_out) if return_lse else out
 
 

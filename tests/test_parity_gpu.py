@@ -179,6 +179,23 @@ def test_host_tensors_end_to_end():
     compare(o.double().numpy(), lse.double().numpy(), o_ref, lse_ref, what="host")
 
 
+@pytest.mark.parametrize("shape", [(4, 8, 2048, 128, 8, True), (1, 16, 8192, 128, 4, False)],
+                         ids=["batch-pieces", "head-group-pieces"])
+def test_host_tensors_in_pieces(shape):
+    """Host problems of 64 MB and more go in pieces on two streams (along the batch, or along
+    the key/value heads of one batch); the result is the one device call's, bit for bit."""
+    from exact_scaled_dot_attn_gb300 import api
+    B, H, N, d, Hkv, causal = shape
+    q, k, v, kl = synth.draw_ex(B, H, Hkv, N, N, d, seed=15, key_len_range=(N // 2, N))
+    assert api._host_pieces(torch.from_numpy(q), torch.from_numpy(k)) is not None
+    tq, tk, tv = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+    o_h, l_h = api.fwd(tq, tk, tv, causal=causal, key_lengths=torch.from_numpy(kl), return_lse=True)
+    o_d, l_d = api.fwd(tq.cuda(), tk.cuda(), tv.cuda(), causal=causal,
+                       key_lengths=torch.from_numpy(kl).cuda(), return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
 def test_non_default_stream():
     from exact_scaled_dot_attn_gb300 import api
     q, k, v, _ = synth.draw(1, 2, 257, 64, seed=15)
