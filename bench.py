@@ -540,40 +540,11 @@ def variants(torch, api, peaks, peak_src):
                                   "unit": "TFLOP/s", "frac": tf / peak,
                                   "peak_source": f"{peak_src} bf16 dense burst"}}
         del qd, kd, vd, od
-    # decoding (one query per sequence, grouped heads): HBM-bound, GB/s of Q, K, V read and O
-    # written once; the tiled kernel alone and split-KV with the automatic split count
-    w = synth.WORKLOADS["decode_gqa"]
-    q, k, v, _ = synth.draw_workload(w)
-    qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
-    od = torch.empty_like(qd)
-    nbytes = synth.min_bytes_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d)
-    n_splits = int(api._lib.lib().attn_splitkv_auto_splits_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d,
-                                                               int(w.causal)))
-    ws = torch.empty(api.splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits), dtype=torch.uint8,
-                     device="cuda")
-
-    def dec_plain():
-        api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od)
-
-    def dec_split():
-        api.fwd_splitkv(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od, n_splits=n_splits,
-                        workspace=ws)
-
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    res = {}
-    for nm, fn in (("plain", dec_plain), ("split", dec_split)):
-        time_launches(torch, fn, 3, flush)
-        res[nm] = statistics.median(time_launches(torch, fn, 30, flush))
-    gbs = {nm: nbytes / (ms * 1e-3) / 1e9 for nm, ms in res.items()}
-    out["decode_gqa"] = {"workload": w.describe(), "value": gbs["split"], "unit": "GB/s",
-                         "launch_ms": res["split"], "n_splits": n_splits, "bytes": nbytes,
-                         "unsplit_value": gbs["plain"], "unsplit_launch_ms": res["plain"],
-                         "kernel": "tcgen05 (query heads of a group packed into one tile)",
-                         "roofline": {"bound": "hbm", "achieved": gbs["split"], "peak": hbm,
-                                      "unit": "GB/s", "frac": gbs["split"] / hbm,
-                                      "peak_source": f"{peak_src} copy bandwidth"},
-                         "timing": "single launches after the L2 flush; split includes the merge kernel"}
-    del qd, kd, vd, od, ws
+    # decoding (one query, or a block of draft queries, per sequence, grouped heads): HBM-bound,
+    # GB/s of Q, K, V read and O written once; the tiled kernel alone and split-KV with the
+    # automatic split count
+    for dname in ("decode_gqa", "spec_decode"):
+        out[dname] = decode_line(torch, api, peaks, peak_src, flush, synth.WORKLOADS[dname])
 
     # fp32 inputs at the reranking shape: HBM-bound, GB/s of Q, K, V read and O written once
     w = synth.WORKLOADS["rerank_f32"]
@@ -598,6 +569,39 @@ def variants(torch, api, peaks, peak_src):
     out["l2"] = "flushed (512 MiB write) before every timed launch"
     return out
 
+
+def decode_line(torch, api, peaks, peak_src, flush, w):
+    """One decoding workload: the tiled kernel alone and split-KV (automatic count), GB/s of Q,
+    K, V read and O written once, single launches after the L2 flush."""
+    q, k, v, _ = synth.draw_workload(w)
+    qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
+    od = torch.empty_like(qd)
+    nbytes = synth.min_bytes_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d)
+    n_splits = int(api._lib.lib().attn_splitkv_auto_splits_ex(w.B, w.H, w.H_kv, w.N, w.N_k, w.d,
+                                                               int(w.causal)))
+    ws = torch.empty(api.splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits), dtype=torch.uint8,
+                     device="cuda")
+
+    def plain():
+        api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od)
+
+    def split():
+        api.fwd_splitkv(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od, n_splits=n_splits,
+                        workspace=ws)
+
+    res = {}
+    for name, fn in (("plain", plain), ("split", split)):
+        time_launches(torch, fn, 3, flush)
+        res[name] = statistics.median(time_launches(torch, fn, 30, flush))
+    gbs = {name: nbytes / (ms * 1e-3) / 1e9 for name, ms in res.items()}
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"workload": w.describe(), "value": gbs["split"], "unit": "GB/s", "launch_ms": res["split"],
+            "n_splits": n_splits, "bytes": nbytes, "unsplit_value": gbs["plain"],
+            "unsplit_launch_ms": res["plain"],
+            "kernel": "tcgen05 (query heads of a group packed into one tile)",
+            "roofline": {"bound": "hbm", "achieved": gbs["split"], "peak": hbm, "unit": "GB/s",
+                         "frac": gbs["split"] / hbm, "peak_source": f"{peak_src} copy bandwidth"},
+            "timing": "single launches after the L2 flush; split includes the merge kernel"}
 
 if __name__ == "__main__":
     sys.exit(main())

@@ -1093,6 +1093,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tO = lane_base + C::tmem_o(t, b);
             const int row = U.q0 + t * kBM + rt;
             const int tile_row0 = U.q0 + t * kBM;
+            // causal: this row's last allowed key, and the key past which some row of the tile
+            // needs the element mask (fixed for the unit)
+            const int row_diag = (p.qrows ? row % p.qrows : row) + qdiag;
+            const int mask_from = p.qrows ? qdiag : tile_row0 + diag;
             float m_ref = -INFINITY; // reference max of the exponentials (log2 units)
             float l = 0.f;
             for (int j = 0; j < n_kv; ++j) {
@@ -1103,11 +1107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++s_it;
                 tc_fence_after();
                 const int kv0 = (U.j0 + j) * kBN;
-                const bool need_mask = (kv0 + kBN > U.L) ||
-                                       (p.causal && kv0 + kBN - 1 > (p.qrows ? qdiag : tile_row0 + diag));
+                const bool need_mask = (kv0 + kBN > U.L) || (p.causal && kv0 + kBN - 1 > mask_from);
                 int lim = U.L - kv0; // keys [kv0, kv0 + lim) are allowed for this row
                 if (p.causal)
-                    lim = min(lim, (p.qrows ? row % p.qrows : row) + qdiag - kv0 + 1);
+                    lim = min(lim, row_diag - kv0 + 1);
 
                 uint32_t sv[kBN];
                 tmem_ld128(tS, sv);

@@ -90,6 +90,8 @@ WORKLOADS = {
     # decoding one token per sequence over a cache of 8192 keys, 32 query heads over 8 key/value
     # heads (the diagonal of the causal mask leaves every key to the one query)
     "decode_gqa": Workload("decode_gqa", 8, 32, 1, 128, True, seed=11, Hkv=8, Nk=8192),
+    # a block of 8 draft queries per sequence (speculative decoding) over 8192 keys, causal
+    "spec_decode": Workload("spec_decode", 8, 32, 8, 128, True, seed=12, Hkv=8, Nk=8192),
     # the prefill shape with bf16 inputs
     "prefill_bf16": Workload("prefill_bf16", 4, 32, 4096, 128, True, seed=9, dtype="bf16"),
     # the reranking shape with fp32 inputs (the precision of the reranker's own kernel)
