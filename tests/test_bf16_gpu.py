@@ -25,6 +25,8 @@ CASES = [
     (2, 8, 2, 300, 700, 128, True, None),
     (1, 4, 1, 640, 200, 64, True, [200]),
     (2, 4, 2, 65, 65, 32, False, None),
+    (2, 8, 2, 4, 500, 64, True, [500, 77]),    # causal draft block, query groups packed
+    (3, 8, 4, 1, 700, 128, True, None),        # one query per sequence, packed
 ]
 
 

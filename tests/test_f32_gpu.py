@@ -24,6 +24,7 @@ CASES = [
     (2, 2, 2, 300, 300, True, None),
     (2, 8, 2, 200, 517, True, [517, 100]),
     (1, 4, 1, 640, 130, False, None),
+    (2, 8, 2, 5, 400, True, [400, 33]),        # causal draft block, query groups packed
 ]
 
 
