@@ -8,8 +8,10 @@ forward over the whole batch with inputs resident in HBM. The same line carries:
   short_n      the reranking workload (B=50, H=12, N=256, d=32, key padding) in GB/s of
                minimum traffic, inputs rotated over buffer sets larger than L2
   split_kv     one long causal head, the tiled kernel alone and with split-KV
-  variants     grouped-query prefill (32 query heads over 8 key/value heads), a block of
-               1024 queries over 16384 cached keys, and the prefill shape in bf16, in TFLOP/s
+  variants     the long (N=32768) and stress (d=64, peaked rows) workloads, grouped-query
+               prefill (32 query heads over 8 key/value heads), a block of 1024 queries over
+               16384 cached keys and the prefill shape in bf16 in TFLOP/s; decoding, a block of
+               draft queries and fp32 reranking in GB/s
   roofline     the dominant kernel's achieved FLOP/s against the measured peak
   cpu_baseline the fp64 oracle timed on the host cores on a bounded sample (rank 0, N=1)
   clocks       SM clocks and throttle reasons sampled during the timed region
@@ -521,7 +523,7 @@ def variants(torch, api, peaks, peak_src):
     flush = l2_flush_buffer(torch)
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     out = {}
-    for name in ("gqa_prefill", "chunk_prefill", "prefill_bf16"):
+    for name in ("long", "stress", "gqa_prefill", "chunk_prefill", "prefill_bf16"):
         w = synth.WORKLOADS[name]
         q, k, v, _ = synth.draw_workload(w)
         qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
@@ -532,7 +534,7 @@ def variants(torch, api, peaks, peak_src):
             api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od)
 
         time_launches(torch, fn, 3, flush)
-        ms = statistics.median(time_launches(torch, fn, 30, flush))
+        ms = statistics.median(time_launches(torch, fn, 10 if name == "long" else 30, flush))
         tf = flops / (ms * 1e-3) / 1e12
         out[name] = {"workload": w.describe(), "value": tf, "unit": "TFLOP/s", "launch_ms": ms,
                      "kernel": "tcgen05", "dtype": w.dtype,
