@@ -86,9 +86,22 @@ struct ShortArgs {
 
 // The heads of this CTA: position pos of the global order (longest first) goes to CTA
 // pos mod G in rounds that alternate direction, so the longest heads spread over the grid.
+// A CTA takes its rounds last to first, i.e. its shortest head first: the first loads of all
+// CTAs, which run before any CTA can compute, are then as small as they can be, and the
+// longer heads load while the first is computed.
 struct HeadCursor {
-    long long round;
+    long long round; // next round to take; -1 when done
 };
+
+__device__ __forceinline__ HeadCursor first_head(const ShortArgs &a)
+{
+    const long long G = gridDim.x;
+    const long long c = blockIdx.x;
+    long long r = (a.n_heads + G - 1) / G - 1; // last round
+    while (r >= 0 && r * G + ((r & 1) ? (G - 1 - c) : c) >= a.n_heads)
+        --r;
+    return HeadCursor{r};
+}
 
 __device__ __forceinline__ int clamp_len(int L, int N) { return L < 0 ? 0 : (L > N ? N : L); }
 
@@ -97,10 +110,10 @@ __device__ __forceinline__ bool next_head(const ShortArgs &a, const int *s_len, 
 {
     const long long G = gridDim.x;
     const long long c = blockIdx.x;
-    const long long r = cur.round++;
-    const long long pos = r * G + ((r & 1) ? (G - 1 - c) : c);
-    if (pos >= a.n_heads)
+    const long long r = cur.round--;
+    if (r < 0)
         return false;
+    const long long pos = r * G + ((r & 1) ? (G - 1 - c) : c);
     const int H = a.p.H;
     const int rank = static_cast<int>(pos / H);
     const int h = static_cast<int>(pos - static_cast<long long>(rank) * H);
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // operands); one elected lane issues each TMA copy, tcgen05.mma and commit.
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        HeadCursor cur{0};
+        HeadCursor cur = first_head(args);
         int bh, L;
         uint32_t hc = 0; // heads loaded
         while (next_head(args, s_len, s_inv, cur, bh, L)) {
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         constexpr uint32_t kLboK = (16u >> 4) << 16;                                 // K-major: unused
         constexpr uint32_t kLboV = (static_cast<uint32_t>(C::kTileBytes) >> 4) << 16; // one atom wide: unused
         auto desc = [](uint32_t lo) -> uint64_t { return (static_cast<uint64_t>(kDescHi) << 32) | lo; };
-        HeadCursor cur{0};
+        HeadCursor cur = first_head(args);
         int bh, L;
         uint32_t hc = 0;        // heads with work
         uint32_t k = 0;         // tiles issued
@@ -411,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 fail();
             return r;
         };
-        HeadCursor cur{0};
+        HeadCursor cur = first_head(args);
         int bh, L;
         uint32_t k = 0;
         while (ok && next_head(args, s_len, s_inv, cur, bh, L)) {
