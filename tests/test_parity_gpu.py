@@ -73,6 +73,30 @@ def test_scales(scale, d):
         compare(o, lse, o_ref, lse_ref, what=f"{kern} scale={scale}")
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("sign", [1.0, -1.0], ids=["pos", "neg"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_growing_scores_move_reference(d, sign, causal):
+    """Scores that grow by about 2^12 per 128-key tile: every later tile's exponentials against
+    the row's reference overflow fp16, so each one is redone with the row max. Rows alternate
+    the sign of q, so in every warp half the rows grow and half shrink (the warp redoes a tile
+    for some rows only); a negative scale mirrors it."""
+    B, H, N = 1, 2, 640
+    rng = np.random.Generator(np.random.PCG64(4242 + d))
+    step = 12.0 / (math.sqrt(d) * 1.4426950408889634)  # per-tile growth of k: +12 in log2 units
+    t = (np.arange(N) // 128).astype(np.float64)
+    k = (step * t)[None, None, :, None] * (1.0 + 0.05 * rng.standard_normal((B, H, N, d)))
+    s = np.where(np.arange(N) % 2 == 0, 1.0, -1.0)[None, None, :, None]
+    q = s * (1.0 + 0.05 * rng.standard_normal((B, H, N, d)))
+    v = rng.standard_normal((B, H, N, d))
+    q, k, v = (x.astype(np.float16) for x in (q, k, v))
+    scale = sign / math.sqrt(d)
+    o_ref, lse_ref = oracle_full(q, k, v, causal=causal, sm_scale=scale)
+    for kern in kernels_for(d, N):
+        o, lse = run_gpu(q, k, v, causal=causal, sm_scale=scale, path=kern)
+        compare(o, lse, o_ref, lse_ref, what=f"{kern} d={d} sign={sign} causal={causal}")
+
+
 def _workload_case(name):
     w = synth.WORKLOADS[name]
     q, k, v, kl = synth.draw_workload(w)
