@@ -5,9 +5,10 @@
 //
 // At N <= 256 a 128-row Q tile sees at most 256 keys, so its whole score row S = Q K^T fits
 // in Tensor Memory (256 fp32 columns) at once. The softmax of "Self-Attention Kernel &
-// Inference Engine from Scratch" ("Online Softmax Formulation") then needs a single step:
-// the row max over all allowed keys is known before any exponential, the running
-// normaliser is one sum, and the accumulator is never rescaled. The per-block skip of
+// Inference Engine from Scratch" ("Online Softmax Formulation") then takes one pass over the
+// row: the exponentials are taken block by block against a reference from the row's first
+// block (moved, with the P already written, only when a block would leave fp16's range), and
+// the accumulator is written once, by one PV product over the final P. The per-block skip of
 // keys past the sequence's length (the "cuda-reranker" README's padding tile skip) is
 // applied to the loads as well: K and V are fetched only up to key_lengths[b], in 32-row
 // boxes, and the S product is only as wide as the allowed keys (rounded up to 16).
@@ -48,6 +49,7 @@ constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 256; // per CTA: two CTAs per SM share the 512 columns
 constexpr int kMaxSortB = 512;      // batches sorted by key length on the device (more: natural order)
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kGuessSumMax = 32768.0f; // a block whose p sum to at most this has every p < 2^16
 
 template <int D> struct SCfg {
     static constexpr int kRowBytes = D * 2;               // 64 B (d = 32) or 128 B: one swizzle row
@@ -458,11 +460,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc_fence_after();
                 // One pass over the row in 64-column blocks. The exponentials use a reference
-                // m_ref that moves only when a block's max exceeds it by more than 2^8 (so every
-                // p <= 256 fits fp16); when it moves, l and the P blocks already written are
-                // rescaled by 2^(m_old - m_new). O is accumulated afterwards from the final P, so
-                // the result is exact. Every decision around the warp-collective TMEM accesses
-                // is made uniform across the warp.
+                // m_ref taken from the first block's max; it moves only when a block's max
+                // exceeds it by more than 2^8 (a later block is checked through its sum, see
+                // below, so every p stays inside fp16); when it moves, l and the P blocks already
+                // written are rescaled by 2^(m_old - m_new). O is accumulated afterwards from the
+                // final P, so the result is exact. Every decision around the warp-collective TMEM
+                // accesses is made uniform across the warp.
                 const bool neg = scale < 0.f;
                 const float fill = neg ? INFINITY : -INFINITY;
                 const uint64_t sc2 = f2_pack(scale, scale);
@@ -492,44 +495,75 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int i = 0; i < 64; ++i)
                             v[i] = i < r ? v[i] : __float_as_uint(fill);
                     }
-                    const float braw = neg ? chunk_ext<32, true>(v, chunk_ext<0, true>(v, INFINITY))
-                                           : chunk_ext<32, false>(v, chunk_ext<0, false>(v, -INFINITY));
-                    const float bm = braw == fill ? -INFINITY : braw * scale; // block max (log2 units)
-                    const bool move = bm > m_ref + 8.f;
-                    const bool any_move = __any_sync(0xffffffffu, move);
-                    float alpha = 1.f;
-                    if (any_move) {
-                        const float m_new = move ? bm : m_ref;
-                        alpha = ex2_approx(m_ref - m_new); // 0 on the first block
-                        const uint64_t a2 = f2_pack(alpha, alpha);
+                    // After the first block every row has a reference (its first key is always
+                    // allowed), so a later block is first exponentiated against it without a
+                    // block max: when the block's sum stays <= 2^15 every p fits fp16 and the
+                    // block is kept; otherwise it is redone with the block max (its scores are
+                    // still in v, and P never overwrites the scores of the block being written).
+                    bool guess = b > 0;
+#pragma unroll 1
+                    for (;;) {
+                        bool any_move = false;
+                        float alpha = 1.f;
+                        if (!guess) {
+                            const float braw = neg ? chunk_ext<32, true>(v, chunk_ext<0, true>(v, INFINITY))
+                                                   : chunk_ext<32, false>(v, chunk_ext<0, false>(v, -INFINITY));
+                            const float bm = braw == fill ? -INFINITY : braw * scale; // block max (log2 units)
+                            const bool move = bm > m_ref + 8.f;
+                            any_move = __any_sync(0xffffffffu, move);
+                            if (any_move) {
+                                const float m_new = move ? bm : m_ref;
+                                alpha = ex2_approx(m_ref - m_new); // 0 on the first block
+                                const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    acc[i] = f2_fma(acc[i], a2, f2_pack(0.f, 0.f));
+                                m_ref = m_new;
+                            }
+                        }
+                        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+                        uint64_t bacc[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            acc[i] = f2_fma(acc[i], a2, f2_pack(0.f, 0.f));
-                        m_ref = m_new;
-                    }
-                    const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
-                    if (full)
-                        exp_chunk<0, true>(v, 64, sc2, nm2, acc, pk);
-                    else
-                        exp_chunk<0, false>(v, r, sc2, nm2, acc, pk);
-                    tmem_st16(lane_base + b * 32, pk);
-                    if (full)
-                        exp_chunk<32, true>(v, 64, sc2, nm2, acc, pk);
-                    else
-                        exp_chunk<32, false>(v, r - 32, sc2, nm2, acc, pk);
-                    tmem_st16(lane_base + b * 32 + 16, pk);
-                    if (any_move && b > 0) {
-                        // the P blocks written with the old reference are rescaled (fp16 pairs)
-                        tmem_wait_st();
-                        const uint32_t ah = pack_f16x2(alpha, alpha);
-                        for (int pb = 0; pb < b; ++pb) {
-                            uint32_t w[32];
-                            tmem_ld32(lane_base + pb * 32, w);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                w[i] = hmul2(w[i], ah);
-                            tmem_st32(lane_base + pb * 32, w);
+                            bacc[i] = f2_pack(0.f, 0.f);
+                        if (full)
+                            exp_chunk<0, true>(v, 64, sc2, nm2, bacc, pk);
+                        else
+                            exp_chunk<0, false>(v, r, sc2, nm2, bacc, pk);
+                        tmem_st16(lane_base + b * 32, pk);
+                        if (full)
+                            exp_chunk<32, true>(v, 64, sc2, nm2, bacc, pk);
+                        else
+                            exp_chunk<32, false>(v, r - 32, sc2, nm2, bacc, pk);
+                        tmem_st16(lane_base + b * 32 + 16, pk);
+                        if (guess) {
+                            float s0, s1, s2, s3;
+                            f2_unpack(f2_add(bacc[0], bacc[1]), s0, s1);
+                            f2_unpack(f2_add(bacc[2], bacc[3]), s2, s3);
+                            const float bs = (s0 + s1) + (s2 + s3);
+                            if (__any_sync(0xffffffffu, !(bs <= kGuessSumMax))) {
+                                tmem_wait_st(); // the redo's stores land after these
+                                guess = false;
+                                continue;
+                            }
                         }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            acc[i] = f2_add(acc[i], bacc[i]);
+                        if (any_move && b > 0) {
+                            // the P blocks written with the old reference are rescaled (fp16 pairs)
+                            tmem_wait_st();
+                            const uint32_t ah = pack_f16x2(alpha, alpha);
+                            for (int pb = 0; pb < b; ++pb) {
+                                uint32_t w[32];
+                                tmem_ld32(lane_base + pb * 32, w);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    w[i] = hmul2(w[i], ah);
+                                tmem_st32(lane_base + pb * 32, w);
+                            }
+                        }
+                        break;
                     }
                 }
                 float a0, a1, b0, b1;

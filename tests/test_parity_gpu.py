@@ -75,16 +75,18 @@ def test_scales(scale, d):
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("sign", [1.0, -1.0], ids=["pos", "neg"])
+@pytest.mark.parametrize("N,period", [(640, 128), (256, 64)], ids=["N640", "N256"])
 @pytest.mark.parametrize("d", [32, 64, 128])
-def test_growing_scores_move_reference(d, sign, causal):
-    """Scores that grow by about 2^12 per 128-key tile: every later tile's exponentials against
-    the row's reference overflow fp16, so each one is redone with the row max. Rows alternate
-    the sign of q, so in every warp half the rows grow and half shrink (the warp redoes a tile
-    for some rows only); a negative scale mirrors it."""
-    B, H, N = 1, 2, 640
-    rng = np.random.Generator(np.random.PCG64(4242 + d))
-    step = 12.0 / (math.sqrt(d) * 1.4426950408889634)  # per-tile growth of k: +12 in log2 units
-    t = (np.arange(N) // 128).astype(np.float64)
+def test_growing_scores_move_reference(d, N, period, sign, causal):
+    """Scores that grow by about 2^12 per block of `period` keys (the tiled kernels' 128-key
+    tiles, the short kernel's 64-column blocks): every later block's exponentials against the
+    row's reference would leave fp16, so the reference moves on every block. Rows alternate the
+    sign of q, so in every warp half the rows grow and half shrink (the warp moves for some rows
+    only); a negative scale mirrors it."""
+    B, H = 1, 2
+    rng = np.random.Generator(np.random.PCG64(4242 + d + N))
+    step = 12.0 / (math.sqrt(d) * 1.4426950408889634)  # per-block growth of k: +12 in log2 units
+    t = (np.arange(N) // period).astype(np.float64)
     k = (step * t)[None, None, :, None] * (1.0 + 0.05 * rng.standard_normal((B, H, N, d)))
     s = np.where(np.arange(N) % 2 == 0, 1.0, -1.0)[None, None, :, None]
     q = s * (1.0 + 0.05 * rng.standard_normal((B, H, N, d)))
