@@ -274,7 +274,9 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S)
     return static_cast<size_t>(total);
 }
 
-// Ranges per (batch*head, Q tile pair) for the automatic choice. Without the causal mask every
+// Ranges per (batch*head, Q tile pair) for the automatic choice. When every pair has the same
+// K/V tile count and balanced runs over all pairs finish sooner than any equal split, the
+// ranges those runs need (attn::splitkv_balanced_auto). Otherwise: without the causal mask every
 // (pair, range) unit has the same length, so the most ranges that still give one unit per SM
 // (floor(SMs / pairs)) shorten the launch without adding a second wave. With it, enough units
 // that the largest is no longer than an SM's average share: the largest pair's K/V tile count
@@ -282,6 +284,10 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S)
 // times SMs / pairs, rounded up. At most one range per two K/V tiles, at most kMaxSplits.
 int auto_splits(int B, int H, int Nq, int Nk, int causal, int sms)
 {
+    // balanced runs over all pairs, where they finish sooner than any equal split
+    const int bal = attn::splitkv_balanced_auto(B * H, Nq, Nk, causal, sms, kMaxSplits);
+    if (bal > 0)
+        return bal;
     const int n_pairs = (Nq + 255) / 256;
     const long long pairs = static_cast<long long>(B) * H * n_pairs;
     long long want;

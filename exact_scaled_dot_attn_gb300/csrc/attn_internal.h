@@ -50,6 +50,16 @@ cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int
 cudaError_t launch_tcgen05_splitkv(const FwdParams &p, int n_splits, float *opart, float *lpart,
                                    cudaStream_t stream, unsigned int *status);
 
+// Balanced split-KV: when every (batch*head, Q tile pair) has the same K/V tile count (no
+// causal mask, or a single pair), the tiles of all pairs are laid end to end and cut into one
+// equal run per SM, each run one or two units; range s of a pair is its part of the s-th run
+// that touches it. splitkv_balanced_runs: the per-pair tile count when a launch with n_splits
+// ranges per pair uses these runs (they fit and finish sooner than equal ranges), else 0.
+// splitkv_balanced_auto: the ranges per pair to ask for when balanced runs beat every equal
+// split up to max_splits, else 0. (B*H, N and causal as the kernels run them.)
+int splitkv_balanced_runs(int BH, int N, int Nk, int causal, int sms, int n_splits);
+int splitkv_balanced_auto(int BH, int N, int Nk, int causal, int sms, int max_splits);
+
 // Persistent short-sequence kernel (self-attention only: Nk = N <= 256, Hkv = H, d in {32, 64}).
 cudaError_t launch_short(const FwdParams &p, cudaStream_t stream, unsigned int *status);
 

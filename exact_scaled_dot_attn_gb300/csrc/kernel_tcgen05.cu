@@ -161,6 +161,11 @@ struct TcArgs {
     int n_units; // n_pairs * B * H * n_splits
     int head_block; // heads per L2 block of the unit order
     int n_splits;   // key ranges per (batch*head, Q tile pair); 1 outside split-KV
+    // Balanced split-KV (bal_chunks > 0): the K/V tiles of all (batch*head, pair) units, bal_nfull
+    // per pair, laid end to end and cut into bal_chunks equal runs (one per CTA); range s of a
+    // pair is its part of the s-th run that touches it (empty when there is none).
+    int bal_chunks;
+    int bal_nfull;
     float *opart;   // split-KV partial outputs: [split][B*H*N][D] fp32, O / l of the range
     float *lpart;   // split-KV partial logsumexp: [split][B*H*N] fp32 (-inf: no key in the range)
     unsigned int *status;
@@ -223,8 +228,22 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs &a, int u)
     const int full1 = U.q0 + kBM < a.p.N ? (kv_end1 + kBN - 1) / kBN : 0;
     const int n_full = max(full0, full1);
     // Key range of this split: K/V tiles [j0, j1) of the pair's n_full tiles.
-    const int j0 = split * n_full / S;
-    const int j1 = (split + 1) * n_full / S;
+    int j0 = split * n_full / S;
+    int j1 = (split + 1) * n_full / S;
+    if (a.bal_chunks > 0) {
+        // run c covers tiles [c T / G, (c + 1) T / G) of the T laid end to end; the pair (w-th in
+        // the unit order, one head block) starts at tile w * nf, inside run c0
+        const long long nf = a.bal_nfull, G = a.bal_chunks;
+        const long long T = static_cast<long long>(BH) * a.n_pairs * nf;
+        const long long t0 = static_cast<long long>(w) * nf;
+        const long long c = ((t0 + 1) * G - 1) / T + split;
+        const long long lo = c * T / G, hi = (c + 1) * T / G;
+        const long long a0 = lo > t0 ? lo : t0, a1 = hi < t0 + nf ? hi : t0 + nf;
+        j0 = c < G && a0 < a1 ? static_cast<int>(a0 - t0) : 0;
+        j1 = c < G && a0 < a1 ? static_cast<int>(a1 - t0) : 0;
+        j1 = min(j1, n_full); // past the keys this pair really has (key lengths)
+        j0 = min(j0, j1);
+    }
     U.j0 = j0;
     U.split = split;
     U.n_kv_t[0] = max(0, min(j1, full0) - j0);
@@ -1230,6 +1249,100 @@ int head_block_for(int BH, int Nk, int D, int G)
     return static_cast<int>(hblk < 1 ? 1 : (hblk > BH ? BH : hblk));
 }
 
+// Run (of G over T tiles laid end to end, run c covering [c T / G, (c + 1) T / G)) that holds
+// tile t.
+long long run_of(long long t, long long T, long long G) { return ((t + 1) * G - 1) / T; }
+
+// K/V tiles per (batch*head, pair) as the host sees them (key lengths taken as Nk), when every
+// pair has the same count (no causal mask, or a single pair); 0 otherwise.
+int uniform_pair_tiles(int N, int Nk, int causal)
+{
+    const int n_pairs = (N + 2 * kBM - 1) / (2 * kBM);
+    if (!causal)
+        return (Nk + kBN - 1) / kBN;
+    if (n_pairs != 1)
+        return 0;
+    const int e0 = std::max(0, std::min(Nk, kBM + Nk - N));
+    const int e1 = std::max(0, std::min(Nk, 2 * kBM + Nk - N));
+    const int f0 = (e0 + kBN - 1) / kBN;
+    const int f1 = kBM < N ? (e1 + kBN - 1) / kBN : 0;
+    return std::max(f0, f1);
+}
+
+// Longest run of K/V tiles (in tiles, plus a per-unit cost) a CTA gets: balanced runs of
+// ceil(T / G) tiles, each starting ceil(run / nf) + 1 units at most, or equal ranges of a
+// pair in waves.
+// Cost of a unit start in K/V tiles, fitted on GB300 decode shapes (d = 128, 8192 keys, 32 query
+// heads over 8): balanced runs were faster at 108 tiles per SM (188 vs 209 us) and slower at
+// 27-47 (70 vs 67 us), which puts it between 5 and 20.
+constexpr long long kUnitCostTiles = 8;
+long long balanced_makespan(long long pairs, int nf, int G)
+{
+    const long long T = pairs * nf;
+    const long long run = (T + G - 1) / G;
+    return run + ((run + nf - 1) / nf + 1) * kUnitCostTiles;
+}
+long long uniform_makespan(long long pairs, int nf, int sms, int S)
+{
+    const long long units = pairs * S;
+    const long long waves = (units + sms - 1) / sms;
+    return waves * ((nf + S - 1) / S + kUnitCostTiles);
+}
+
+// Most runs that touch one pair (the ranges per pair a balanced split needs).
+int balanced_slots(long long pairs, int nf, int G)
+{
+    const long long T = pairs * nf;
+    long long mx = 0;
+    for (long long w = 0; w < pairs; ++w)
+        mx = std::max(mx, run_of(w * nf + nf - 1, T, G) - run_of(w * nf, T, G) + 1);
+    return static_cast<int>(mx);
+}
+
+} // namespace
+
+// Balanced split-KV for a launch with n_splits ranges per pair: the per-pair K/V tile count
+// when the balanced runs fit in n_splits ranges, fit the schedule table and finish sooner than
+// n_splits equal ranges per pair; 0 for the equal ranges.
+int splitkv_balanced_runs(int BH, int N, int Nk, int causal, int sms, int n_splits)
+{
+    const int nf = uniform_pair_tiles(N, Nk, causal);
+    if (nf < 2 || n_splits < 2 || sms < 1)
+        return 0;
+    const long long pairs = static_cast<long long>(BH) * ((N + 2 * kBM - 1) / (2 * kBM));
+    const long long T = pairs * nf;
+    const int G = static_cast<int>(T < sms ? T : sms);
+    if (G > kMaxCtas || pairs * n_splits > kMaxSchedUnits || pairs > 0xffff)
+        return 0;
+    if (balanced_slots(pairs, nf, G) > n_splits)
+        return 0;
+    return balanced_makespan(pairs, nf, G) < uniform_makespan(pairs, nf, sms, n_splits) ? nf : 0;
+}
+
+// Ranges per pair for the automatic split-KV choice when balanced runs beat every equal split
+// (the slots they need), else 0.
+int splitkv_balanced_auto(int BH, int N, int Nk, int causal, int sms, int max_splits)
+{
+    const int nf = uniform_pair_tiles(N, Nk, causal);
+    if (nf < 2 || sms < 1)
+        return 0;
+    const long long pairs = static_cast<long long>(BH) * ((N + 2 * kBM - 1) / (2 * kBM));
+    const long long T = pairs * nf;
+    const int G = static_cast<int>(T < sms ? T : sms);
+    const int slots = balanced_slots(pairs, nf, G);
+    if (slots < 2 || slots > max_splits)
+        return 0;
+    long long best_uniform = uniform_makespan(pairs, nf, sms, 1);
+    for (int S = 2; S <= max_splits && S <= nf; ++S)
+        best_uniform = std::min(best_uniform, uniform_makespan(pairs, nf, sms, S));
+    return splitkv_balanced_runs(BH, N, Nk, causal, sms, slots) > 0 &&
+                   balanced_makespan(pairs, nf, G) < best_uniform
+               ? slots
+               : 0;
+}
+
+namespace {
+
 // Largest-first assignment of the units to the least loaded CTA. The units are taken in
 // the device's unit order (head block by head block, heaviest pair first inside a
 // block, the key ranges of a pair next to each other), so every CTA works on the same head
@@ -1281,15 +1394,44 @@ void build_schedule(SchedTable &t, int BH, int N, int Nk, int causal, int head_b
     t.off[grid] = static_cast<uint16_t>(k);
 }
 
+// Balanced split-KV schedule (see TcArgs::bal_chunks): CTA c takes, in order, the part of
+// every pair that run c touches; the ranges a pair has no run for are empty units (they
+// write the zero-weight partials the merge expects), taken by the CTA of the pair's last run.
+void build_balanced_schedule(SchedTable &t, long long pairs, int nf, int G, int S)
+{
+    const long long T = pairs * nf;
+    std::vector<std::vector<uint16_t>> lists(G);
+    for (int c = 0; c < G; ++c) {
+        const long long lo = c * T / G, hi = (c + 1) * T / G;
+        if (lo >= hi)
+            continue;
+        for (long long w = lo / nf; w <= (hi - 1) / nf; ++w)
+            lists[c].push_back(static_cast<uint16_t>(w * S + (c - run_of(w * nf, T, G))));
+    }
+    for (long long w = 0; w < pairs; ++w) {
+        const long long c0 = run_of(w * nf, T, G), c1 = run_of(w * nf + nf - 1, T, G);
+        for (long long k = c1 - c0 + 1; k < S; ++k)
+            lists[c1].push_back(static_cast<uint16_t>(w * S + k));
+    }
+    t.use = 1;
+    int k = 0;
+    for (int c = 0; c < G; ++c) {
+        t.off[c] = static_cast<uint16_t>(k);
+        for (uint16_t u : lists[c])
+            t.unit[k++] = u;
+    }
+    t.off[G] = static_cast<uint16_t>(k);
+}
+
 // Schedules are cached per shape (they depend on B*H, N, Nk, the head block, causal, the
-// split count and the SM count only).
+// split count, the SM count and the balanced run length only).
 std::mutex g_sched_mutex;
-std::map<std::tuple<int, int, int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
+std::map<std::tuple<int, int, int, int, int, int, int, int>, std::shared_ptr<SchedTable>> g_sched_cache;
 
 std::shared_ptr<SchedTable> schedule_for(int BH, int N, int Nk, int causal, int head_block, int n_pairs,
-                                         int n_splits, int grid)
+                                         int n_splits, int grid, int bal_nfull = 0)
 {
-    auto key = std::make_tuple(BH, N, Nk, causal, head_block, n_splits, grid);
+    auto key = std::make_tuple(BH, N, Nk, causal, head_block, n_splits, grid, bal_nfull);
     std::lock_guard<std::mutex> lock(g_sched_mutex);
     auto it = g_sched_cache.find(key);
     if (it != g_sched_cache.end())
@@ -1297,7 +1439,9 @@ std::shared_ptr<SchedTable> schedule_for(int BH, int N, int Nk, int causal, int 
     auto t = std::make_shared<SchedTable>();
     memset(t.get(), 0, sizeof(SchedTable));
     const long long n_units = static_cast<long long>(BH) * n_pairs * n_splits;
-    if (grid <= kMaxCtas && n_units <= kMaxSchedUnits)
+    if (bal_nfull > 0)
+        build_balanced_schedule(*t, static_cast<long long>(BH) * n_pairs, bal_nfull, grid, n_splits);
+    else if (grid <= kMaxCtas && n_units <= kMaxSchedUnits)
         build_schedule(*t, BH, N, Nk, causal, head_block, n_pairs, n_splits, grid);
     if (g_sched_cache.size() >= 64)
         g_sched_cache.clear();
@@ -1345,9 +1489,21 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
         return err;
     if (static_cast<long long>(fa.numRegs) * kThreads < RegSplit<D>::kPoolNeeded)
         return cudaErrorInvalidConfiguration;
-    const int grid = a.n_units < sms ? a.n_units : sms;
-    std::shared_ptr<SchedTable> sched =
-        schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block, a.n_pairs, n_splits, grid);
+    a.bal_chunks = 0;
+    a.bal_nfull = 0;
+    int grid = a.n_units < sms ? a.n_units : sms;
+    if (SPLIT) {
+        const int nf = splitkv_balanced_runs(BH, p.N, p.Nk, p.causal && !p.qrows, sms, n_splits);
+        if (nf > 0) {
+            const long long T = static_cast<long long>(a.n_pairs) * BH * nf;
+            a.bal_nfull = nf;
+            a.bal_chunks = static_cast<int>(T < sms ? T : sms);
+            a.head_block = BH; // one head block: unit u is pair u / S, range u % S
+            grid = a.bal_chunks;
+        }
+    }
+    std::shared_ptr<SchedTable> sched = schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block,
+                                                     a.n_pairs, n_splits, grid, a.bal_nfull);
     kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
     return cudaGetLastError();
 }

@@ -174,6 +174,11 @@ attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, 
  * Scratch" ("Online Softmax Formulation") applied to n_splits ranges at once: with lse_s the
  * logsumexp of range s and O_s its normalised output, lse = log sum_s exp(lse_s) and
  * O = sum_s exp(lse_s - lse) O_s.
+ * Where every pair has the same number of key tiles (no causal mask, or N <= 256) and it
+ * finishes sooner, the ranges are not equal parts of each pair: the key tiles of all pairs are
+ * laid end to end and cut into one equal run per SM, and range s of a pair is its part of the
+ * s-th run that touches it (a pair then has at most n_splits ranges, some possibly empty). The
+ * result is the same attention either way.
  *   n_splits         1..16, or <= 0 for attn_splitkv_auto_splits(B, H, N, d, causal)
  *   workspace        device memory of at least attn_splitkv_workspace_bytes(B, H, N, d, n_splits)
  *                    bytes, 16-byte aligned, owned by the caller; its contents on entry do not
@@ -193,7 +198,9 @@ attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void
 size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 
 /* The split count attn_fwd_splitkv uses for n_splits <= 0, for the current device's SM count:
- * without a causal mask the most ranges that still give one (Q tile pair, key range) unit per
+ * where every pair has the same key tile count and runs of equal length over all pairs (see
+ * attn_fwd_splitkv) finish sooner than any equal split, the most runs that touch one pair;
+ * otherwise, without a causal mask the most ranges that still give one (Q tile pair, key range) unit per
  * SM (SMs / pairs, rounded down); with it enough units that the largest is no longer than an
  * SM's average share (the largest pair's K/V tile count over the mean, about two, times SMs /
  * pairs, rounded up). At most one range per two 128-key tiles and at most 16; at least 1. -1

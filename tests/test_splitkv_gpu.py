@@ -107,3 +107,41 @@ def test_splitkv_one_head_workload_sampled():
     o, lse = run_splitkv(q, k, v, causal=w.causal, n_splits=0)
     assert not np.isnan(o).any()
     compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, what="one_head splitkv")
+
+
+BALANCED = [
+    # B, H, H_kv, N_q, N_k, d, causal, ragged key lengths
+    (32, 32, 8, 1, 8192, 128, True, False),
+    (32, 32, 8, 1, 8192, 128, True, True),
+]
+
+
+@pytest.mark.parametrize("case", BALANCED, ids=["decode", "decode-ragged"])
+def test_splitkv_balanced_runs_decode(case):
+    """A decoding batch large enough that the automatic split lays the key tiles of all
+    (head, pair) units end to end and cuts them into one equal run per SM (two ranges per pair
+    where an equal split would take one): every row against the oracle. Ragged key lengths
+    leave ranges past a batch's keys empty."""
+    B, H, Hkv, Nq, Nk, d, causal, ragged = case
+    assert _lib.lib().attn_splitkv_auto_splits_ex(B, H, Hkv, Nq, Nk, d, int(causal)) >= 2
+    q, k, v, _ = synth.draw_ex(B, H, Hkv, Nq, Nk, d, seed=2100 + int(ragged))
+    kl = None
+    if ragged:
+        rng = np.random.Generator(np.random.PCG64(2102))
+        kl = rng.integers(1, Nk + 1, size=B).astype(np.int32)
+        kl[0], kl[1] = 1, Nk
+    o_ref, lse_ref = oracle_full(q, k, v, causal=causal, key_lengths=kl)
+    o, lse = run_splitkv(q, k, v, causal=causal, key_lengths=kl, n_splits=0)
+    compare(o, lse, o_ref, lse_ref, what=f"balanced decode ragged={ragged}")
+
+
+def test_splitkv_balanced_runs_single_pair_causal():
+    """Causal self-attention with one Q tile pair per head (every pair sees the same key tiles)
+    at a size where the automatic split may use balanced runs; sampled rows."""
+    B, H, N, Nk, d = 8, 16, 200, 8192, 128
+    q, k, v, _ = synth.draw_ex(B, H, H, N, Nk, d, seed=2110)
+    rows = sample_rows(B, H, N, seed=2111, per_head=16)
+    o_ref, lse_ref = oracle.attn(q, k, v, sm_scale=d ** -0.5, causal=True, rows=rows)
+    o, lse = run_splitkv(q, k, v, causal=True, n_splits=0)
+    assert not np.isnan(o).any()
+    compare(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, what="balanced causal pair")
