@@ -628,6 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
+    // Programmatic dependent launch: the setup above overlaps the end of the previous
+    // kernel of the stream; no global memory is touched before griddep_wait.
+    griddep_launch_dependents();
+    griddep_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1504,7 +1508,19 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
     }
     std::shared_ptr<SchedTable> sched = schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block,
                                                      a.n_pairs, n_splits, grid, a.bal_nfull);
-    kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(a, mq, mk, mv, *sched);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, a, mq, mk, mv, *sched);
+    if (err != cudaSuccess)
+        return err;
     return cudaGetLastError();
 }
 
