@@ -39,6 +39,15 @@
  * CUDA call. Kernels that wait on on-chip barriers bound every wait; a wait that
  * runs out ends the block early and records ATTN_ERR_TIMEOUT in a per-device
  * status word that attn_read_device_status() returns.
+ *
+ * Stream order: the tiled and short-sequence kernels use programmatic dependent launch.
+ * Their set-up (barrier initialisation, Tensor Memory allocation) may overlap the end of
+ * the previous kernel on the stream, but they read and write no global memory before that
+ * kernel has completed. Ordering against earlier work is therefore that of an ordinary
+ * launch. They also let the next kernel on the stream start early. A kernel that the
+ * caller launches right after them with programmatic stream serialization must call
+ * cudaGridDependencySynchronize() (griddepcontrol.wait) before it reads O or lse.
+ * Ordinary launches need nothing.
  */
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
