@@ -68,7 +68,7 @@ template <int D> struct SCfg {
 
 // Barrier block (8 bytes each).
 template <int D> struct SBars {
-    static constexpr int kQKFull = 0;                          // [slot] Q tiles and K of a head
+    static constexpr int kQKFull = 0;                          // [slot] Q tile 0 and K of a head
     static constexpr int kVFull = kQKFull + SCfg<D>::kSlots;   // [slot] V of a head
     static constexpr int kSlotFree = kVFull + SCfg<D>::kSlots; // [slot] the head's last MMA is done
     static constexpr int kSFull = kSlotFree + SCfg<D>::kSlots; // S of the current tile is in TMEM
@@ -76,7 +76,8 @@ template <int D> struct SBars {
     static constexpr int kOFull = kPFull + 1;                  // O of the current tile is done
     static constexpr int kOFree = kOFull + 1;                  // O of the current tile was read
     static constexpr int kMmaDone = kOFree + 1;
-    static constexpr int kCount = kMmaDone + 1;
+    static constexpr int kQ1Full = kMmaDone + 1;               // [slot] Q tile 1 of a head
+    static constexpr int kCount = kQ1Full + SCfg<D>::kSlots;
 };
 
 struct ShortArgs {
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(bar(BB::kQKFull + s), 1);
             mbar_init(bar(BB::kVFull + s), 1);
             mbar_init(bar(BB::kSlotFree + s), 1);
+            mbar_init(bar(BB::kQ1Full + s), 1);
         }
         mbar_init(bar(BB::kSFull), 1);
         mbar_init(bar(BB::kPFull), kBM);
@@ -303,18 +305,30 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int q_rows = min(n_qt * kBM, N);
             const int nqb = (q_rows + kBoxRows - 1) / kBoxRows;
             const int nkv = (L + kBoxRows - 1) / kBoxRows;
+            // The first score tile needs only Q tile 0 and K: they go first, under their own
+            // barrier, then Q tile 1 and V (the first wave of loads is HBM-bound).
+            constexpr int kTileBoxes = kBM / kBoxRows;
+            const int nqb0 = nqb < kTileBoxes ? nqb : kTileBoxes;
             if (elect_one()) {
                 const uint32_t qk_bar = bar(BB::kQKFull + slot);
+                const uint32_t q1_bar = bar(BB::kQ1Full + slot);
                 const uint32_t v_bar = bar(BB::kVFull + slot);
-                mbar_arrive_expect_tx(qk_bar, (nqb + nkv) * C::kBoxBytes);
+                mbar_arrive_expect_tx(qk_bar, (nqb0 + nkv) * C::kBoxBytes);
 #pragma unroll
-                for (int i = 0; i < kMaxN / kBoxRows; ++i)
-                    if (i < nqb)
+                for (int i = 0; i < kTileBoxes; ++i)
+                    if (i < nqb0)
                         tma_load_3d(sQ + i * C::kBoxBytes, &tm_q, qk_bar, 0, i * kBoxRows, bh);
 #pragma unroll
                 for (int i = 0; i < kMaxN / kBoxRows; ++i)
                     if (i < nkv)
                         tma_load_3d(sK + i * C::kBoxBytes, &tm_k, qk_bar, 0, i * kBoxRows, bh);
+                if (nqb > kTileBoxes) {
+                    mbar_arrive_expect_tx(q1_bar, (nqb - kTileBoxes) * C::kBoxBytes);
+#pragma unroll
+                    for (int i = kTileBoxes; i < kMaxN / kBoxRows; ++i)
+                        if (i < nqb)
+                            tma_load_3d(sQ + i * C::kBoxBytes, &tm_q, q1_bar, 0, i * kBoxRows, bh);
+                }
                 mbar_arrive_expect_tx(v_bar, nkv * C::kBoxBytes);
 #pragma unroll
                 for (int i = 0; i < kMaxN / kBoxRows; ++i)
@@ -328,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0)
             for (uint32_t i = hc > C::kSlots ? hc - C::kSlots : 0; i < hc; ++i) {
                 mbar_wait(bar(BB::kQKFull + i % C::kSlots), (i / C::kSlots) & 1u, nullptr, kWaitLimitNs);
+                if (n_qt > 1)
+                    mbar_wait(bar(BB::kQ1Full + i % C::kSlots), (i / C::kSlots) & 1u, nullptr, kWaitLimitNs);
                 mbar_wait(bar(BB::kVFull + i % C::kSlots), (i / C::kSlots) & 1u, nullptr, kWaitLimitNs);
             }
         __syncwarp();
@@ -369,6 +385,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         break;
                     o_pending = false;
                 }
+                if (t == 1 && !wait(bar(BB::kQ1Full + slot), ph))
+                    break;
                 tc_fence_after();
                 const uint32_t qlo = ((sQ + t * kBM * C::kRowBytes) >> 4) | kLboK;
                 const uint32_t klo = (sK >> 4) | kLboK;
