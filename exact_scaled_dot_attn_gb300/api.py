@@ -41,7 +41,8 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
     key_lengths: int32 [B]; keys j >= key_lengths[b] are excluded.
     sm_scale: defaults to 1/sqrt(d).
     return_lse: also return the fp32 [B, H, N] logsumexp.
-    path: "auto", "warp_mma" or "tcgen05" (kernel choice; see include/attn.h).
+    path: "auto", "warp_mma", "tcgen05" or "short" (kernel choice; see include/attn.h;
+    "short" takes N <= 256 with d in {32, 64}).
     Device tensors run asynchronously on the current stream. CPU tensors are
     copied to the current CUDA device and back, and the call returns after the
     copy back has finished.
