@@ -443,6 +443,9 @@ extern "C" attn_status_t attn_fwd_splitkv_noalloc(const void *q, const void *k, 
         n_splits = attn_splitkv_auto_splits(B, H, N, d, causal);
         if (n_splits < 1)
             return ATTN_ERR_INVALID_ARG;
+        // the automatic count, lowered to the most ranges whose partials fit the array
+        while (n_splits > 1 && splitkv_bytes(B, H, N, d, n_splits) > kNoAllocScratchBytes)
+            --n_splits;
     }
     if (n_splits > kMaxSplits)
         return ATTN_ERR_INVALID_ARG;

@@ -12,9 +12,10 @@
 // Cross-attention and grouped-query attention: the K/V rows come from the query
 // head's key/value head (Nk keys), and the causal diagonal moves by Nk - N.
 //
-// This kernel serves every head dimension and length; it is the path for short
-// sequences and d = 32, where the work is bound by memory traffic, not by the
-// tensor pipe. Long sequences at d in {64, 128} run on the tcgen05 kernel.
+// This kernel serves every head dimension and length but is on no automatic path: the
+// tcgen05 kernels are faster at every measured shape (the short-sequence kernel for d = 32
+// with N <= 256, the tiled kernel elsewhere). It is kept as an independent second
+// implementation that is selected explicitly (ATTN_PATH_WARP_MMA) and run by the parity tests.
 #include "attn_internal.h"
 
 #include <math.h>

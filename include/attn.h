@@ -30,7 +30,9 @@
  * probabilities are rounded to fp16 before the PV product.
  *
  * Ownership: the caller owns every buffer. The entry points allocate no memory,
- * keep no per-call state and are safe to call from several host threads.
+ * keep no per-call state and are safe to call from several host threads, with one
+ * exception: attn_fwd_splitkv_noalloc shares one fixed scratch array per GPU among all
+ * its calls, and its declaration states how such calls must be ordered.
  *
  * Errors: argument errors are returned synchronously, before anything is
  * launched. Launch failures return ATTN_ERR_CUDA. The work is asynchronous on
@@ -243,12 +245,19 @@ int attn_splitkv_auto_splits_ex(int B, int H, int H_kv, int N_q, int N_k, int d,
  * pay the synchronisation of cudaMalloc/cudaFree. It is attn_fwd_splitkv with its workspace
  * in a fixed array of attn_noalloc_scratch_bytes() bytes (64 MiB) that is part of the
  * library's device code: every GPU on which the library is loaded holds that array until the
- * process exits. The caller passes inputs and outputs only; nothing is allocated, by this
- * library or by any library it calls.
+ * process exits. The caller passes inputs and outputs only; no call allocates, in this
+ * library or in any library it calls.
+ *   - n_splits <= 0 takes the automatic count (attn_splitkv_auto_splits), lowered to the
+ *     largest count whose workspace fits the array.
  *   - A problem whose split-KV workspace (attn_splitkv_workspace_bytes) exceeds the array
- *     returns ATTN_ERR_SCRATCH_LIMIT before any launch; use fewer splits or attn_fwd_splitkv.
- *   - The first call on a device looks up the array's device address (once per device, with
- *     that device current); make that first call before any stream capture.
+ *     (for the automatic count: even with one range) returns ATTN_ERR_SCRATCH_LIMIT before
+ *     any launch; use fewer splits or attn_fwd_splitkv.
+ *   - The array belongs to the library's device code. The CUDA driver reserves it on a GPU
+ *     when it loads that code there, which with lazy module loading (the default) happens at
+ *     the first call of this entry point on the device, not when the library is opened. The
+ *     same first call looks up the array's device address (once per device, with that device
+ *     current). A caller that must not see any reservation on its hot path makes one warm-up
+ *     call on each device first, outside any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's contents (no
  *     part of it needs clearing: each call writes all it reads). Calls whose executions overlap
  *     on the same GPU (different streams, concurrent host threads) race on it and must be

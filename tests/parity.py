@@ -174,8 +174,9 @@ def oracle_full(q, k, v, *, causal, key_lengths=None, sm_scale=None):
 
 
 def sample_rows(B, H, N, seed, per_head=48, heads=None):
-    """Deterministic sample of flat row ids: tile edges, ragged tail and random rows in a few
-    heads (first, last and random ones)."""
+    """Deterministic sample of flat row ids: tile edges, ragged tail and random rows in each of
+    the given flat (batch*head) heads, or by default in a few heads (first, last and random
+    ones)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     BH = B * H
     if heads is None:

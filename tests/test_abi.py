@@ -1,10 +1,12 @@
 """The C-ABI library builds, loads, exports every symbol include/attn.h declares, and rejects
-bad arguments synchronously (CPU only: no call here reaches a CUDA API)."""
+bad arguments synchronously (CPU only: no call here launches a kernel; a few reach a CUDA
+device query, which fails without a GPU)."""
 import ctypes
 import os
 import re
 
 import pytest
+import torch
 
 from exact_scaled_dot_attn_gb300 import _lib, build
 
@@ -134,6 +136,27 @@ def test_noalloc_scratch_limit(lib):
     assert st == _lib.ATTN_ERR_SCRATCH_LIMIT
     assert lib.attn_fwd_splitkv_noalloc(A, A, A, A, None, 1, 1, 256, 64, 0.125, 0, None, 17,
                                         None) == _lib.ATTN_ERR_INVALID_ARG
+    # the automatic count cannot fit when even one range overflows the array
+    assert lib.attn_splitkv_workspace_bytes(B, H, N, d, 1) > cap
+    st = lib.attn_fwd_splitkv_noalloc(A, A, A, A, None, B, H, N, d, 0.088, 1, None, 0, None)
+    assert st == _lib.ATTN_ERR_SCRATCH_LIMIT
+
+
+def test_noalloc_auto_count_lowered_to_fit(lib):
+    """With n_splits <= 0 the no-allocation entry point lowers the automatic count until the
+    partials fit its array: here the automatic count (2 ranges on the 148-SM count assumed
+    without a GPU) needs more than the array and one range fits, so the call gets past the
+    scratch check (and, with no GPU, fails at the device lookup). Skipped where a GPU is
+    present: the call would launch on the fake pointers."""
+    if torch.cuda.is_available():
+        pytest.skip("would launch on fake device pointers")
+    cap = lib.attn_noalloc_scratch_bytes()
+    B, H, N, d = 1, 4, 16384, 128
+    auto = lib.attn_splitkv_auto_splits(B, H, N, d, 1)
+    assert auto >= 2 and lib.attn_splitkv_workspace_bytes(B, H, N, d, auto) > cap
+    assert lib.attn_splitkv_workspace_bytes(B, H, N, d, 1) <= cap
+    st = lib.attn_fwd_splitkv_noalloc(A, A, A, A, None, B, H, N, d, 0.088, 1, None, 0, None)
+    assert st == _lib.ATTN_ERR_CUDA
 
 
 def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=64, dtype=0,

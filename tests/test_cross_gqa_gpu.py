@@ -104,18 +104,14 @@ def test_short_path_refuses_cross_shapes():
 
 
 @pytest.mark.parametrize("name", ["gqa_prefill", "chunk_prefill"])
-def test_gqa_workload_sampled_rows(name):
-    """The grouped-query workloads at full size; rows sampled in a few heads (the oracle
-    computes them one by one)."""
+def test_gqa_workload_all_rows(name):
+    """The grouped-query workloads at full size, every row against the oracle."""
     w = synth.WORKLOADS[name]
     q, k, v, kl = synth.draw_workload(w)
-    rows = sample_rows(w.B, w.H, w.N, seed=w.seed, per_head=40)
-    o_ref, lse_ref = oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal, key_lengths=kl,
-                                 rows=rows)
+    o_ref, lse_ref = oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal, key_lengths=kl)
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     o, lse = api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, return_lse=True)
     assert api.read_device_status() == _lib.ATTN_OK
     o = o.double().cpu().numpy()
     lse = lse.double().cpu().numpy()
-    assert not np.isnan(o).any()
-    compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, what=name)
+    compare(o, lse, o_ref, lse_ref, what=name)

@@ -1,10 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element.
 
 Small shapes run the whole output through the oracle; they span several tiles of every
-kernel and end in ragged tails. The five measured workloads run at full size: the tiny and
-reranking ones are compared on every row, the long ones on sampled rows the oracle computes
-one by one. Analytic cases (uniform keys, one-hot selection, causal row 0, empty rows) are
-checked against their closed forms on the GPU too.
+kernel and end in ragged tails. The five measured workloads run at full size: the tiny,
+reranking, prefill and stress ones are compared on every row (the reranking workload ignores
+its padded query rows), the long one (whose full oracle would take minutes) on tile-edge and
+random rows in every one of its heads. Analytic cases (uniform keys, one-hot selection, causal
+row 0, empty rows) are checked against their closed forms on the GPU too.
 """
 import math
 
@@ -105,34 +106,46 @@ def _workload_case(name):
     return w, q, k, v, kl
 
 
-@pytest.mark.parametrize("name", ["tiny", "rerank"])
+def _workload_kernels(w):
+    """The automatic choice, then every other kernel that takes the shape (the automatic one
+    is not launched twice)."""
+    from exact_scaled_dot_attn_gb300 import api
+    auto = api.auto_path(w.N, w.d)
+    return ["auto"] + [k for k in kernels_for(w.d, w.N) if k != auto]
+
+
+@pytest.mark.parametrize("name", ["tiny", "rerank", "prefill", "stress"])
 def test_workload_full_rows(name):
+    """Every row of the workload against the oracle (the stress workload checks lse too, as
+    every comparison here does); the padded query rows of the reranking workload are the
+    only rows left out."""
     w, q, k, v, kl = _workload_case(name)
     o_ref, lse_ref = oracle_full(q, k, v, causal=w.causal, key_lengths=kl)
     row_mask = None
     if w.ignore_padded_queries:
         i = np.arange(w.N)[None, None, :]
         row_mask = np.broadcast_to(i < kl[:, None, None], (w.B, w.H, w.N))
-    for kern in ["auto"] + kernels_for(w.d, w.N):
+    for kern in _workload_kernels(w):
         o, lse = run_gpu(q, k, v, causal=w.causal, key_lengths=kl, path=kern)
         compare(o, lse, o_ref, lse_ref, row_mask=row_mask, what=f"{name} {kern}")
+        if w.causal:
+            # causal row 0 of every head: O_0 = V_0 up to the fp16 rounding of the output
+            assert np.max(np.abs(o[:, :, 0] - v[:, :, 0].astype(np.float64))) <= 1e-3
 
 
-@pytest.mark.parametrize("name", ["prefill", "stress", "long"])
-def test_workload_sampled_rows(name):
-    w, q, k, v, kl = _workload_case(name)
-    rows = sample_rows(w.B, w.H, w.N, seed=w.seed, per_head=24)
+def test_long_workload_rows_in_every_head():
+    """The long workload (N = 32768, causal) at full size: tile-edge rows, the ragged end and
+    24 random rows in every one of its 32 heads, which the oracle computes one by one."""
+    w, q, k, v, kl = _workload_case("long")
+    rows = sample_rows(w.B, w.H, w.N, seed=w.seed, per_head=24, heads=range(w.B * w.H))
     o_ref, lse_ref = oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal,
                                  key_lengths=kl, rows=rows)
-    for kern in ["auto"] + kernels_for(w.d, w.N):
+    for kern in _workload_kernels(w):
         o, lse = run_gpu(q, k, v, causal=w.causal, key_lengths=kl, path=kern)
         o_s = o.reshape(-1, w.d)[rows]
         lse_s = lse.reshape(-1)[rows]
-        assert not np.isnan(o).any(), f"{name} {kern}: unwritten rows"
-        compare(o_s, lse_s, o_ref, lse_ref, what=f"{name} {kern}")
-        if not w.causal:
-            continue
-        # causal row 0 of every head: O_0 = V_0 exactly up to fp16 rounding of the output
+        assert not np.isnan(o).any(), f"long {kern}: unwritten rows"
+        compare(o_s, lse_s, o_ref, lse_ref, what=f"long {kern}")
         assert np.max(np.abs(o[:, :, 0] - v[:, :, 0].astype(np.float64))) <= 1e-3
 
 
