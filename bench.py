@@ -52,11 +52,12 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05", "short"])
+    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05", "short", "naive"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short-n", action="store_true")
     ap.add_argument("--no-split-kv", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-naive", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
 
@@ -296,7 +297,16 @@ def main():
     od = torch.empty_like(qd)
     flops = synth.attention_flops_ex(w.B, w.H, w.N, w.N_k, w.d, w.causal)
 
+    naive_ws = None
+    if args.path == "naive":
+        naive_ws = torch.empty(api.naive_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8,
+                               device="cuda")
+
     def step():
+        if naive_ws is not None:
+            api.fwd_naive(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld,
+                          out=od, workspace=naive_ws)
+            return
         api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od,
                 path=args.path)
 
@@ -334,21 +344,23 @@ def main():
     ms_per_step = region_ms / steps
     value = weak_scaling_value(world, flops, ms_per_step * 1e-3)
 
+    del naive_ws
     # End to end through the public API with host tensors.
     e2e_steps = max(1, min(args.e2e_steps, steps))
     tq, tk, tv = (to_host(torch, x, w.dtype).pin_memory() for x in (q, k, v))
     tkl = torch.from_numpy(kl) if kl is not None else None
     o_host = torch.empty(q.shape, dtype=tq.dtype, pin_memory=True)
+    e2e_path = "auto" if args.path == "naive" else args.path  # (the host-tensor API is fused only)
     for _ in range(2):
         api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
-                path=args.path)
+                path=e2e_path)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
-                path=args.path)
+                path=e2e_path)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, device="cuda")
     h2d = sum(x.nbytes for x in (q, k, v)) + (kl.nbytes if kl is not None else 0)
@@ -365,6 +377,13 @@ def main():
                 "frac": achieved / peak, "traffic": traffic_from_profile(kernel_name, w.name),
                 "kernel": kernel_name, "peak_source": f"{peak_src} bf16 dense burst (fp16 rate = bf16 rate)",
                 "avg_launch_ms": avg_launch_ms}
+    if args.path == "naive":
+        # the three passes are bound by the traffic of the materialised S and P
+        gbs = naive_model_bytes(w) / (avg_launch_ms * 1e-3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": traffic_from_profile("naive", w.name), "kernel": "naive (three passes)",
+                    "peak_source": f"{peak_src} copy bandwidth", "avg_launch_ms": avg_launch_ms}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
@@ -373,7 +392,7 @@ def main():
         "config": dict(workload_config(w), path=args.path, kernel=kernel_name),
         "e2e": {"value": weak_scaling_value(world, flops, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": steps,
+        "gpu_launches": steps * (3 if args.path == "naive" else 1),
         "roofline": roofline,
         "clocks": clocks,
     }
@@ -384,6 +403,8 @@ def main():
         line["split_kv"] = split_kv(torch, api, peaks, peak_src)
     if not args.no_variants:
         line["variants"] = variants(torch, api, peaks, peak_src)
+    if not args.no_naive:
+        line["naive"] = naive_lines(torch, api, peaks, peak_src)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # Bounded sample of the same workload: the first heads (flat batch*head order), all
@@ -569,6 +590,73 @@ def variants(torch, api, peaks, peak_src):
                                       "frac": gbs / hbm, "peak_source": f"{peak_src} copy bandwidth"},
                          "timing": "single launches, each after the L2 flush (launch latency included)"}
     out["l2"] = "flushed (512 MiB write) before every timed launch"
+    return out
+
+
+def naive_model_bytes(w):
+    """Algorithmic bytes of one naive forward as the three passes run it: S (fp32) written
+    once and read once, P (fp16) written once and read once, over the padded [B*H, N, Np]
+    matrices, plus Q and K read by pass 1, V read by pass 3, O written and the lse (fp32)
+    written once."""
+    np_cols = (w.N + 127) // 128 * 128
+    elems = w.B * w.H * w.N * np_cols
+    return 12 * elems + 8 * w.B * w.H * w.N * w.d + 4 * w.B * w.H * w.N
+
+
+def pages_model_bytes(w):
+    """The naive page's count of the five-step pipeline's traffic per head, 7 S^2 + 4 S d
+    fp16 elements ("Naive Attention Kernel", section "2. HBM Traffic Analysis"), in bytes
+    over every head."""
+    return w.B * w.H * (7 * w.N * w.N + 4 * w.N * w.d) * 2
+
+
+def naive_lines(torch, api, peaks, peak_src):
+    """The naive three-pass forward (S and P through HBM) against the fused kernel on the
+    workloads it serves: per-launch time (median, L2 flushed before each launch), the
+    algorithmic bytes of its three passes and the achieved rate of them against the measured
+    copy bandwidth, the page's traffic model, the measured DRAM bytes of one launch (the three
+    kernels, from the committed ncu summary while the source matches), and its time over the
+    fused kernel's."""
+    flush = l2_flush_buffer(torch)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    names = ("tiny", "rerank", "prefill", "stress")
+    ws = torch.empty(max(api.naive_workspace_bytes(synth.WORKLOADS[n].B, synth.WORKLOADS[n].H,
+                                                   synth.WORKLOADS[n].N) for n in names),
+                     dtype=torch.uint8, device="cuda")
+    out = {}
+    for name in names:
+        w = synth.WORKLOADS[name]
+        q, k, v, kl = synth.draw_workload(w)
+        qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+        kld = torch.from_numpy(kl).cuda() if kl is not None else None
+        od = torch.empty_like(qd)
+
+        def naive():
+            api.fwd_naive(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld,
+                          out=od, workspace=ws)
+
+        def fused():
+            api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od)
+
+        res = {}
+        for label, fn in (("naive", naive), ("fused", fused)):
+            time_launches(torch, fn, 3, flush)
+            res[label] = statistics.median(time_launches(torch, fn, 10, flush))
+        nbytes = naive_model_bytes(w)
+        gbs = nbytes / (res["naive"] * 1e-3) / 1e9
+        flops = synth.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+        out[name] = {"workload": w.describe(), "launch_ms": res["naive"],
+                     "fused_launch_ms": res["fused"], "naive_over_fused": res["naive"] / res["fused"],
+                     "value": flops / (res["naive"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                     "model_bytes": nbytes, "pages_model_bytes": pages_model_bytes(w),
+                     "fused_min_bytes": synth.min_bytes(w.B, w.H, w.N, w.d),
+                     "dram_bytes_measured": traffic_from_profile("naive", name),
+                     "gpu_launches": 3,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                  "frac": gbs / hbm, "peak_source": f"{peak_src} copy bandwidth"}}
+        del qd, kd, vd, od
+    del ws
+    out["timing"] = "single forwards (three kernels) after the L2 flush; median of 10"
     return out
 
 

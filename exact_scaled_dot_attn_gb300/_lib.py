@@ -54,6 +54,9 @@ SIGNATURES = {
     "attn_fwd_splitkv_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i,
                                  _vp, ctypes.c_size_t, _vp]),
     "attn_splitkv_auto_splits_ex": (_i, [_i, _i, _i, _i, _i, _i, _i]),
+    "attn_fwd_naive": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp,
+                            ctypes.c_size_t, _vp]),
+    "attn_naive_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i]),
 }
 
 _lib = None

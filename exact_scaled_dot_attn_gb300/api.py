@@ -179,6 +179,58 @@ def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, n_splits: int) -> in
     return int(_lib.lib().attn_splitkv_workspace_bytes(B, H, N, d, n_splits))
 
 
+def fwd_naive(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+              sm_scale: float | None = None, key_lengths: torch.Tensor | None = None,
+              return_lse: bool = False, out: torch.Tensor | None = None,
+              lse_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """The naive three-pass forward (attn_fwd_naive): S and P written to and read back from
+    `workspace`, a CUDA tensor of at least naive_workspace_bytes(B, H, N) bytes (allocated here
+    when None). The library's comparison baseline; fp16 self-attention, device tensors only."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("fwd_naive takes CUDA tensors")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_device_tensor(name, t, (B, H, N, d), torch.float16, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_device_tensor("out", out, (B, H, N, d), torch.float16, dev)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, H, N), device=dev,
+                                                               dtype=torch.float32)
+        _check_device_tensor("lse_out", lse, (B, H, N), torch.float32, dev)
+    if key_lengths is not None:
+        _check_device_tensor("key_lengths", key_lengths, (B,), torch.int32, dev)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    L = _lib.lib()
+    need = naive_workspace_bytes(B, H, N)
+    if need == 0:
+        raise ValueError("invalid sizes for the naive forward")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the device of q")
+    with torch.cuda.device(dev):
+        st = L.attn_fwd_naive(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, B, H, N, d, float(sm_scale),
+            int(bool(causal)), key_lengths.data_ptr() if key_lengths is not None else None,
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            torch.cuda.current_stream(dev).cuda_stream)
+    if st != _lib.ATTN_OK:
+        raise _lib.AttnError(st, "attn_fwd_naive")
+    return (out, lse) if return_lse else out
+
+
+def naive_workspace_bytes(B: int, H: int, N: int) -> int:
+    """Workspace bytes fwd_naive needs (0 for invalid sizes)."""
+    return int(_lib.lib().attn_naive_workspace_bytes(B, H, N))
+
+
 # Host problems at least this large (Q, K, V and O together) are copied and computed in pieces.
 _HOST_CHUNK_MIN_BYTES = 64 << 20
 _HOST_PIECES = 8

@@ -386,6 +386,49 @@ extern "C" attn_status_t attn_fwd_splitkv(const void *q, const void *k, const vo
                                key_lengths, n_splits, workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- naive three-pass baseline
+namespace {
+
+// Bytes of the naive pass's workspace: S [B*H][N][Np] fp32, then P [B*H][N][Np] fp16; 0 when
+// the sizes are invalid or the count does not fit size_t.
+size_t naive_bytes(int B, int H, int N)
+{
+    if (B < 1 || H < 1 || N < 1)
+        return 0;
+    const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+    const unsigned long long np = static_cast<unsigned long long>(attn::naive_padded_cols(N));
+    if (rows > (1ull << 40) || np > (1ull << 32))
+        return 0;
+    const unsigned long long elems = rows * np;
+    if (elems / np != rows || elems > static_cast<unsigned long long>(SIZE_MAX) / 6ull)
+        return 0;
+    return static_cast<size_t>(elems * 6ull);
+}
+
+} // namespace
+
+extern "C" size_t attn_naive_workspace_bytes(int B, int H, int N) { return naive_bytes(B, H, N); }
+
+extern "C" attn_status_t attn_fwd_naive(const void *q, const void *k, const void *v, void *o, float *lse,
+                                        int B, int H, int N, int d, float sm_scale, int causal,
+                                        const int32_t *key_lengths, void *workspace,
+                                        size_t workspace_bytes, attn_stream_t stream)
+{
+    attn_status_t st = validate(q, k, v, o, lse, self_shape(B, H, N, d), sm_scale, causal, key_lengths);
+    if (st != ATTN_OK)
+        return st;
+    const size_t need = naive_bytes(B, H, N);
+    if (need == 0 || !workspace || workspace_bytes < need)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16))
+        return ATTN_ERR_MISALIGNED;
+    attn::FwdParams p = make_params(q, k, v, o, lse, self_shape(B, H, N, d), sm_scale, causal, key_lengths);
+    float *s = static_cast<float *>(workspace);
+    __half *pm = reinterpret_cast<__half *>(s + static_cast<size_t>(B) * H * N * attn::naive_padded_cols(N));
+    const cudaError_t err = attn::launch_naive(p, s, pm, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- split-KV without allocation
 //
 // Some callers cannot allocate device memory on the path that calls the attention: a serving

@@ -63,6 +63,12 @@ int splitkv_balanced_auto(int BH, int N, int Nk, int causal, int sms, int max_sp
 // Persistent short-sequence kernel (self-attention only: Nk = N <= 256, Hkv = H, d in {32, 64}).
 cudaError_t launch_short(const FwdParams &p, cudaStream_t stream, unsigned int *status);
 
+// Naive three-pass forward (fp16 self-attention): S = sm_scale Q K^T into s ([B*H][N][Np] fp32),
+// P = softmax(S + mask) into pm ([B*H][N][Np] fp16) with lse, then O = P V. Np =
+// naive_padded_cols(N), N rounded up to a multiple of 128.
+cudaError_t launch_naive(const FwdParams &p, float *s, __half *pm, cudaStream_t stream);
+long long naive_padded_cols(int N);
+
 // Multiprocessor count of the current device (cached per device).
 cudaError_t device_sm_count(int *out);
 

@@ -230,6 +230,36 @@ attn_status_t attn_fwd_splitkv_ex(const void *q, const void *k, const void *v, v
                                   int n_splits, void *workspace, size_t workspace_bytes,
                                   attn_stream_t stream);
 
+/*
+ * Naive three-pass forward: the same attention as attn_fwd_lse, computed the textbook way with
+ * the N x N score and probability matrices written to and read back from device memory ("Naive
+ * Attention Kernel", sections "1. Standard Attention: Step by Step", "2. HBM Traffic Analysis"
+ * and "3. Naive CUDA Implementation"; "Tensor Parallelism with CUDA - Standard Attention",
+ * section "The Naive HBM Algorithm"). It is the library's comparison baseline for the traffic
+ * the fused kernels avoid, not a path for production use:
+ *   pass 1  S = sm_scale * Q K^T for every query/key pair of every head   (fp32, into workspace)
+ *   pass 2  P = softmax(S + mask) row by row, and lse                     (fp16, into workspace)
+ *   pass 3  O = P V over every key column of P                            (fp16, into o)
+ * Scores excluded by the causal mask or the key lengths are computed and stored like the
+ * others; the softmax pass gives them probability 0.
+ *   workspace        device memory of at least attn_naive_workspace_bytes(B, H, N) bytes,
+ *                    16-byte aligned, owned by the caller: S as fp32 [B*H, N, Np], then P as
+ *                    fp16 [B*H, N, Np], with Np = N rounded up to a multiple of 128 (the padded
+ *                    columns of P hold zeros). On return it holds S and P of this call. Launches
+ *                    that share a workspace must not overlap on the device.
+ * fp16 self-attention only ([B, H, N, d], d in {32, 64, 128}); the other arguments, layouts and
+ * errors are those of attn_fwd_lse. A missing or too small workspace gives ATTN_ERR_INVALID_ARG,
+ * a misaligned one ATTN_ERR_MISALIGNED. Three kernel launches on `stream`.
+ */
+attn_status_t attn_fwd_naive(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float sm_scale, int causal,
+                             const int32_t *key_lengths, void *workspace, size_t workspace_bytes,
+                             attn_stream_t stream);
+
+/* Workspace bytes attn_fwd_naive needs: B*H*N*Np*6 (fp32 S and fp16 P, Np = N rounded up to a
+ * multiple of 128); 0 for invalid sizes or a count that does not fit size_t. */
+size_t attn_naive_workspace_bytes(int B, int H, int N);
+
 /* attn_splitkv_auto_splits for the shapes of attn_fwd_ex (H query heads over H_kv key/value heads,
  * N_q query rows over N_k keys), counted on the problem the kernels run (query heads of a group
  * packed together where attn_fwd_ex packs them); under the causal mask the largest pair's work

@@ -173,6 +173,26 @@ def oracle_full(q, k, v, *, causal, key_lengths=None, sm_scale=None):
     return oracle.attn(q, k, v, sm_scale=sm_scale, causal=causal, key_lengths=key_lengths)
 
 
+_WORKLOAD_CACHE: dict = {}
+
+
+def workload_oracle(name):
+    """(w, q, k, v, key_lengths, o_ref, lse_ref) of a named workload with the oracle's output
+    for every row. Computed once per test session and kept for the last four workloads asked
+    for (about 0.7 GB for the prefill and stress workloads together): the large ones take
+    seconds of host time each and several test files compare different kernels with them."""
+    from exact_scaled_dot_attn_gb300 import synth
+    if name not in _WORKLOAD_CACHE:
+        w = synth.WORKLOADS[name]
+        q, k, v, kl = synth.draw_workload(w)
+        o_ref, lse_ref = oracle.attn(q, k, v, sm_scale=w.sm_scale, causal=w.causal,
+                                     key_lengths=kl, dtype=w.dtype)
+        while len(_WORKLOAD_CACHE) >= 4:
+            _WORKLOAD_CACHE.pop(next(iter(_WORKLOAD_CACHE)))
+        _WORKLOAD_CACHE[name] = (w, q, k, v, kl, o_ref, lse_ref)
+    return _WORKLOAD_CACHE[name]
+
+
 def sample_rows(B, H, N, seed, per_head=48, heads=None):
     """Deterministic sample of flat row ids: tile edges, ragged tail and random rows in each of
     the given flat (batch*head) heads, or by default in a few heads (first, last and random

@@ -125,6 +125,35 @@ def test_splitkv_validation(lib):
     assert sk(q=None) == _lib.ATTN_ERR_INVALID_ARG
 
 
+def test_naive_workspace_bytes(lib):
+    # B*H*N*Np*6 with Np = N rounded up to a multiple of 128 (fp32 S, fp16 P)
+    assert lib.attn_naive_workspace_bytes(2, 3, 100) == 2 * 3 * 100 * 128 * 6
+    assert lib.attn_naive_workspace_bytes(4, 32, 4096) == 4 * 32 * 4096 * 4096 * 6
+    assert lib.attn_naive_workspace_bytes(1, 1, 129) == 129 * 256 * 6
+    for bad in [(0, 1, 8), (1, 0, 8), (1, 1, 0), (1, 1, -5)]:
+        assert lib.attn_naive_workspace_bytes(*bad) == 0
+
+
+def test_naive_validation(lib):
+    """Argument errors of the naive forward come back before any launch."""
+    def nv(ws=A, ws_bytes=1 << 30, **kw):
+        args = dict(q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=256, d=64, scale=0.125, causal=0,
+                    kl=None)
+        args.update(kw)
+        return lib.attn_fwd_naive(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                  args["B"], args["H"], args["N"], args["d"], args["scale"],
+                                  args["causal"], args["kl"], ws, ws_bytes, None)
+    need = lib.attn_naive_workspace_bytes(1, 1, 256)
+    assert nv(ws=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert nv(ws_bytes=need - 1) == _lib.ATTN_ERR_INVALID_ARG
+    assert nv(ws=A + 8, ws_bytes=need) == _lib.ATTN_ERR_MISALIGNED
+    assert nv(d=48) == _lib.ATTN_ERR_UNSUPPORTED
+    assert nv(q=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert nv(causal=2) == _lib.ATTN_ERR_INVALID_ARG
+    assert nv(scale=float("nan")) == _lib.ATTN_ERR_INVALID_ARG
+    assert nv(o=A + 2) == _lib.ATTN_ERR_MISALIGNED
+
+
 def test_noalloc_scratch_limit(lib):
     """The no-allocation split-KV entry point states its fixed scratch size and rejects a
     problem that needs more, before any launch."""

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from exact_scaled_dot_attn_gb300 import synth
-from parity import compare, oracle_full, run_gpu, sample_rows
+from parity import compare, oracle_full, run_gpu, sample_rows, workload_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -119,8 +119,7 @@ def test_workload_full_rows(name):
     """Every row of the workload against the oracle (the stress workload checks lse too, as
     every comparison here does); the padded query rows of the reranking workload are the
     only rows left out."""
-    w, q, k, v, kl = _workload_case(name)
-    o_ref, lse_ref = oracle_full(q, k, v, causal=w.causal, key_lengths=kl)
+    w, q, k, v, kl, o_ref, lse_ref = workload_oracle(name)
     row_mask = None
     if w.ignore_padded_queries:
         i = np.arange(w.N)[None, None, :]
