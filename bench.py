@@ -561,6 +561,7 @@ def variants(torch, api, peaks, peak_src):
                      "kernel": "tcgen05", "dtype": w.dtype,
                      "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
                                   "unit": "TFLOP/s", "frac": tf / peak,
+                                  "traffic": traffic_from_profile("tcgen05", name),
                                   "peak_source": f"{peak_src} bf16 dense burst"}}
         del qd, kd, vd, od
     # decoding (one query, or a block of draft queries, per sequence, grouped heads): HBM-bound,
