@@ -185,10 +185,18 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     // tiled tcgen05 kernel only.
     if (path == ATTN_PATH_SHORT && (!sh.self() || sh.Nq > 256 || sh.d > 64))
         return ATTN_ERR_UNSUPPORTED;
-    if (sh.dtype != ATTN_DTYPE_F16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05)
+    // bf16 runs on the tcgen05 kernel only; fp32 on the tcgen05 kernel (TF32 products) or on the
+    // warp-level kernel (split-TF32 products, fp32 accuracy)
+    if (sh.dtype == ATTN_DTYPE_BF16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05)
         return ATTN_ERR_UNSUPPORTED;
-    if (path == ATTN_PATH_AUTO)
-        path = (sh.self() && sh.dtype == ATTN_DTYPE_F16) ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;
+    if (sh.dtype == ATTN_DTYPE_F32 && path == ATTN_PATH_SHORT)
+        return ATTN_ERR_UNSUPPORTED;
+    if (path == ATTN_PATH_AUTO) {
+        if (sh.dtype == ATTN_DTYPE_F32)
+            path = ATTN_PATH_WARP_MMA; // fp32 accuracy
+        else
+            path = (sh.self() && sh.dtype == ATTN_DTYPE_F16) ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;
+    }
 
     attn::FwdParams p = make_params(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (opts && opts->wait_limit_ns)
@@ -204,7 +212,7 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
             err = path == ATTN_PATH_TCGEN05 ? attn::launch_tcgen05(p, s, status)
                                             : attn::launch_short(p, s, status);
     } else {
-        err = attn::launch_warp_mma(p, s);
+        err = sh.dtype == ATTN_DTYPE_F32 ? attn::launch_f32(p, s) : attn::launch_warp_mma(p, s);
     }
     return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -63,6 +63,10 @@ int splitkv_balanced_auto(int BH, int N, int Nk, int causal, int sms, int max_sp
 // Persistent short-sequence kernel (self-attention only: Nk = N <= 256, Hkv = H, d in {32, 64}).
 cudaError_t launch_short(const FwdParams &p, cudaStream_t stream, unsigned int *status);
 
+// fp32 inputs at fp32 accuracy (d = 32): split-TF32 products on the warp-level tensor core
+// instruction, fp32 P and O.
+cudaError_t launch_f32(const FwdParams &p, cudaStream_t stream);
+
 // Naive three-pass forward (fp16 self-attention): S = sm_scale Q K^T into s ([B*H][N][Np] fp32),
 // P = softmax(S + mask) into pm ([B*H][N][Np] fp16) with lse, then O = P V. Np =
 // naive_padded_cols(N), N rounded up to a multiple of 128.

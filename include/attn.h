@@ -77,11 +77,17 @@ typedef enum {
 
 /* Element type of Q, K, V and O for attn_fwd_ex / attn_fwd_splitkv_ex (the other entry points
  * take fp16). bf16 (8-bit exponent, 8-bit significand) runs on the tiled tcgen05 kernel only,
- * with P rounded to bf16 as well: one tcgen05 MMA takes A and B of the same type. fp32
- * (the "cuda-reranker" README's precision, on the tensor cores that README names as its next
- * step) takes fp32 Q, K, V and writes fp32 O, d = 32 only, on the tcgen05 kernel: both
- * products run as TF32 (the tensor core uses the sign, the exponent and the 10 leading fraction
- * bits of each fp32 operand, P included), accumulation and the softmax statistics are fp32. */
+ * with P rounded to bf16 as well: one tcgen05 MMA takes A and B of the same type. fp32 (the
+ * "cuda-reranker" README's precision, on the tensor cores that README names as its next step)
+ * takes fp32 Q, K, V and writes fp32 O, d = 32 only, in one of two ways:
+ *   - ATTN_PATH_AUTO or ATTN_PATH_WARP_MMA: fp32 accuracy. Every operand of both products, P
+ *     included, is split into a TF32 part and a TF32 remainder and each product is formed from
+ *     three TF32 products (error-corrected TF32, Ootomo and Yokota 2022): products within about
+ *     2^-21 of their fp32 value, fp32 accumulation, P never rounded below fp32. Warp-level
+ *     tensor-core kernel (mma.sync m16n8k8 tf32).
+ *   - ATTN_PATH_TCGEN05 (and attn_fwd_splitkv_ex): TF32 products, the tensor core using the
+ *     sign, the exponent and the 10 leading fraction bits of each fp32 operand, P included;
+ *     fp32 accumulation and softmax statistics. Faster, at TF32's precision. */
 typedef enum {
     ATTN_DTYPE_F16 = 0,
     ATTN_DTYPE_BF16 = 1,
@@ -159,12 +165,13 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
  *                N_k - N_q earlier tokens). The pages fix no alignment for N_q != N_k; this is
  *                the reading taken. Rows with no allowed key get O = 0 and lse = -inf.
  *   dtype        attn_dtype_t of q, k, v and o (all four the same): ATTN_DTYPE_F16, or
- *                ATTN_DTYPE_BF16 (tcgen05 kernel only), or ATTN_DTYPE_F32 (tcgen05 kernel,
- *                d = 32 only); another value or d is ATTN_ERR_UNSUPPORTED
+ *                ATTN_DTYPE_BF16 (tcgen05 kernel only), or ATTN_DTYPE_F32 (d = 32 only; see
+ *                attn_dtype_t for its two paths); another value or d is ATTN_ERR_UNSUPPORTED
  *   path         ATTN_PATH_AUTO (for fp16 self-attention shapes the kernel attn_auto_path
- *                selects, the tcgen05 kernel otherwise), ATTN_PATH_TCGEN05 or
- *                ATTN_PATH_WARP_MMA (fp16); ATTN_PATH_SHORT takes fp16 self-attention shapes
- *                only (H_kv = H, N_q = N_k); any other combination is ATTN_ERR_UNSUPPORTED.
+ *                selects, the fp32-accurate kernel for fp32, the tcgen05 kernel otherwise),
+ *                ATTN_PATH_TCGEN05 or ATTN_PATH_WARP_MMA (fp16 and fp32); ATTN_PATH_SHORT
+ *                takes fp16 self-attention shapes only (H_kv = H, N_q = N_k); any other
+ *                combination is ATTN_ERR_UNSUPPORTED.
  * B, H, H_kv, N_q, N_k >= 1 (else ATTN_ERR_INVALID_ARG, as is H not a multiple of H_kv); the
  * element count of every tensor must fit int64 and B*H int32. The other arguments, layouts
  * and errors are those of attn_fwd_lse. With H_kv = H, N_q = N_k and fp16 it is attn_fwd_path.

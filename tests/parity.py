@@ -61,6 +61,46 @@ def tf32_bounds(q, k, v, sm_scale, *, exact_inputs):
     return atol, delta + 1e-4
 
 
+# fp32 inputs at fp32 accuracy (split-TF32 products, the automatic path for fp32): each operand x
+# of both products, P included, is split into hi = x rounded to 10 fraction bits
+# (|x - hi| <= 2^-11 |x|) and lo = x - hi, of which the tensor core reads 10 fraction bits
+# (error <= 2^-10 |lo| <= 2^-21 |x|, truncation assumed); a product is hi*hi + hi*lo + lo*hi,
+# within (2^-21 + 2^-21 + 2^-22) |a b| = SPLIT_U = 5 * 2^-22 of |a b|. Sums are fp32; the tensor
+# core may truncate, so the unit roundoff is taken as ACC_U = 2^-23 and a sum of n terms errs by
+# at most n ACC_U of the sum of their magnitudes (the linear worst case). Per row i, with S_i = max_j sum_c |q_ic||k_jc|:
+#   scores      |ds_ij| <= D_i = |sm_scale| (SPLIT_U + 3 d ACC_U) S_i   (3 d products per score)
+#   exponential relative error <= E_i = 2^-21 + 2^-22 |sm_scale| log2(e) S_i (ex2.approx and the
+#               fp32 rounding of its scaled argument)
+#   weights     P_ij / l_i move by a factor within exp(+-(2 D_i + 2 E_i))
+#   P V         sum_j P_ij v_jc within (SPLIT_U + 3 N_k ACC_U) l_i max_j |v_jc|
+# so |dO_ic| <= (expm1(2 D_i + 2 E_i) + SPLIT_U + 3 N_k ACC_U) max_j |v_jc| + 1e-7 and
+# |dlse_i| <= D_i + 2 E_i + N_k ACC_U + 1e-6. These are worst cases. Independent rounding
+# errors add in quadrature: for scores of a few units (|sm_scale q.k| <~ 10, the normal-scale
+# test inputs and workloads), score errors are ~1e-6 and so are the relative errors of P and O.
+# On such inputs the relative L2 error over a tensor is checked against F32_REL_L2 = 3e-5:
+# thirty times above that estimate and thirty times below TF32's unit roundoff 2^-10, so a
+# result with TF32 products fails it. (With scores in the hundreds, fp32 itself moves the
+# weights by ~1e-4; those cases are checked against the norm of the per-element bounds.)
+SPLIT_U = 5 * 2.0 ** -22
+ACC_U = 2.0 ** -23
+F32_REL_L2 = 3e-5
+
+
+def f32_split_bounds(q, k, v, sm_scale):
+    """(atol [B,H,N,d], lse_tol [B,H,N]) for fp32 inputs on the split-TF32 path (see above)."""
+    q64, k64, v64 = (np.abs(np.asarray(x, dtype=np.float64)) for x in (q, k, v))
+    B, H, N, d = q64.shape
+    n_keys = k64.shape[2]
+    g = H // k64.shape[1]
+    kr = np.repeat(k64, g, axis=1)
+    vmax = np.repeat(v64.max(axis=2, keepdims=True), g, axis=1)  # [B,H,1,d]
+    s_abs = np.einsum("bhid,bhjd->bhij", q64, kr).max(axis=3) if n_keys else np.zeros((B, H, N))
+    delta = abs(sm_scale) * (SPLIT_U + 3 * d * ACC_U) * s_abs
+    eps_e = 2.0 ** -21 + 2.0 ** -22 * abs(sm_scale) * 1.4426950408889634 * s_abs
+    atol = (np.expm1(2 * delta + 2 * eps_e)[..., None] + SPLIT_U + 3 * n_keys * ACC_U) * vmax + 1e-7
+    return atol, delta + 2 * eps_e + n_keys * ACC_U + 1e-6
+
+
 def bf16_to_float(bits):
     """uint16 bfloat16 bit patterns -> float64 (bfloat16 is the upper half of a binary32)."""
     b = np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << 16

@@ -207,7 +207,7 @@ def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=6
     (dict(v=A + 8), _lib.ATTN_ERR_MISALIGNED),
     (dict(dtype=3), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=_lib.DTYPE_F32, d=64), _lib.ATTN_ERR_UNSUPPORTED),   # fp32: d = 32 only
-    (dict(dtype=_lib.DTYPE_F32, d=32, path=_lib.PATH_WARP_MMA), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=_lib.DTYPE_F32, d=32, path=_lib.PATH_SHORT), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=-1), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=_lib.DTYPE_BF16, path=_lib.PATH_WARP_MMA), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=_lib.DTYPE_BF16, Hkv=4, Nk=8, d=32, path=_lib.PATH_SHORT), _lib.ATTN_ERR_UNSUPPORTED),
