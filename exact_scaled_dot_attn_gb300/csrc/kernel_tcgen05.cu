@@ -140,9 +140,15 @@ template <int D, int ES = 2> struct Cfg {
     static constexpr int kVTStages = ES == 4 ? 2 : 0;
     static constexpr int kStages = ES == 4 ? 7 : (kTileBytes >= 32768 ? 5 : (kTileBytes >= 16384 ? 9 : 16)); // K/V ring
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
+    // Separate P (d = 64, 16-bit elements): P_t gets its own 64 TMEM columns instead of the
+    // first half of S_t, so S_t(j+1) is issued as soon as the softmax has read S_t(j), before
+    // O_t += P_t(j) V_j; the softmax of the next step then finds its scores ready. The columns
+    // come from the second O buffer (one O buffer per tile here).
+    static constexpr bool kSepP = D == 64 && ES == 2;
+    static constexpr uint32_t kTmemP0 = 384, kTmemP1 = 448;
     // O accumulators: two per Q tile when they fit (d <= 64), so that a unit's epilogue
     // can read one while the next unit's PV products accumulate into the other.
-    static constexpr int kOBufs = D <= 64 ? 2 : 1;
+    static constexpr int kOBufs = (D <= 64 && !kSepP) ? 2 : 1;
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t tmem_o(int t, int b)
     {
@@ -327,7 +333,9 @@ template <int D, int ES = 2> struct Bars {
     static constexpr int kVReady = kMmaDone + 1;  // [2]
     static constexpr int kVTFull = kVReady + 2;   // [2]
     static constexpr int kVTEmpty = kVTFull + 2;  // [2]
-    static constexpr int kCount = kVTEmpty + 2;
+    // separate P only: the softmax of tile t has read S_t (the next S_t may be written)
+    static constexpr int kSFree = kVTEmpty + 2;   // [2]
+    static constexpr int kCount = kSFree + 2;
 };
 
 // Column chunks of the S row: the allowed columns of a row are a prefix e < lim (key
@@ -610,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(BB::kSFull + t), 1);
             mbar_init(bar(BB::kPFull + t), kBM);
+            mbar_init(bar(BB::kSFree + t), kBM);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(BB::kOReady + i), 1);
@@ -762,7 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K-major in four 32-key blocks of 4 KB, 8 keys (32 bytes) per k-step. (Issued by the
         // elected lane.)
         auto issue_pv = [&](int t, uint32_t v_slot, uint32_t vt, bool accumulate) {
-            const uint32_t a_tmem = tmem + (t ? C::kTmemS1 : C::kTmemS0);
+            const uint32_t a_tmem = C::kSepP ? tmem + (t ? C::kTmemP1 : C::kTmemP0)
+                                             : tmem + (t ? C::kTmemS1 : C::kTmemS0);
             const int b = static_cast<int>((ob >> t) & 1u);
             const uint32_t d_tmem = tmem + C::tmem_o(t, b);
             if constexpr (TF32) {
@@ -817,6 +827,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool have = take_work(U);
         if (have && !start_unit(U))
             have = false;
+        if constexpr (C::kSepP) {
+            // step j: S_t(j+1) = Q_t K_{j+1}^T for every tile as soon as its softmax has read
+            // S_t(j) (SFree), then O_t += P_t(j) V_j once P_t(j) is out. The ring holds K_j, V_j,
+            // K_{j+1}, ... in that order; K_{j+1} is taken before V_j.
+            uint32_t sf_par = 0; // bit t: parity of the SFree waits of tile t
+            while (ok && have) {
+                const uint32_t uq_slot = q_slot;
+                const bool have_next = take_work(Un);
+                for (int j = 0; j < U.n_kv && ok; ++j) {
+                    const uint32_t v_pos = kv_it;
+                    const uint32_t v_slot = v_pos % C::kStages;
+                    const bool has_next = j + 1 < U.n_kv;
+                    const uint32_t k_slot = (v_pos + 1) % C::kStages;
+                    if (has_next) {
+                        bool k_ready = false;
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (j + 1 >= kv_tiles(U, t))
+                                continue;
+                            if (!wait(bar(BB::kSFree + t), (sf_par >> t) & 1u))
+                                break;
+                            sf_par ^= 1u << t;
+                            if (!k_ready) {
+                                if (!wait(bar(BB::kKVFull + k_slot), ((v_pos + 1) / C::kStages) & 1u))
+                                    break;
+                                k_ready = true;
+                            }
+                            tc_fence_after();
+                            if (elect_one())
+                                issue_s(t, k_slot);
+                            __syncwarp();
+                        }
+                        if (!ok)
+                            break;
+                    }
+                    if (!wait(bar(BB::kKVFull + v_slot), (v_pos / C::kStages) & 1u))
+                        break;
+                    kv_it = v_pos + (has_next ? 2u : 1u);
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= kv_tiles(U, t))
+                            continue;
+                        if (j == 0) {
+                            // the epilogue of the unit that last used this tile's O is done
+                            const int ob_i = t * 2;
+                            if (!wait(bar(BB::kOEmpty + ob_i), ((oe_par >> ob_i) & 1u) ^ 1u))
+                                break;
+                            oe_par ^= 1u << ob_i;
+                        }
+                        if (!wait(bar(BB::kPFull + t), (p_par >> t) & 1u))
+                            break;
+                        p_par ^= 1u << t;
+                        tc_fence_after();
+                        if (elect_one())
+                            issue_pv(t, v_slot, 0u, j > 0);
+                        __syncwarp();
+                    }
+                    if (!ok)
+                        break;
+                    if (elect_one()) {
+                        mma_commit(bar(BB::kKVEmpty + v_slot));
+                        if (has_next) {
+                            mma_commit(bar(BB::kKVEmpty + k_slot));
+                            if (j + 2 == U.n_kv)
+                                mma_commit(bar(BB::kQEmpty + uq_slot));
+                        }
+                    }
+                    __syncwarp();
+                    if (!has_next && have_next) {
+                        if (!start_unit(Un))
+                            break;
+                    }
+                }
+                U = Un;
+                have = have_next;
+            }
+            have = false;
+        }
         while (ok && have) {
             const uint32_t uq_slot = q_slot; // this unit's Q buffer
             ob = C::kOBufs == 2 ? u_par : 0u;
@@ -975,6 +1061,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rt = wq * 32 + lane;   // row within the Q tile = TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tS = lane_base + (t ? C::kTmemS1 : C::kTmemS0);
+        // where P_t goes: its own columns (separate P) or over the first half of S_t
+        const uint32_t tP = C::kSepP ? lane_base + (t ? C::kTmemP1 : C::kTmemP0) : tS;
         const float scale = p.scale_log2;
         const int diag = p.Nk - p.N; // causal: query i sees keys j <= i + diag
         // packed query groups: row r is query r % qrows, whose diagonal is at Nk - qrows; every
@@ -1137,6 +1225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 uint32_t sv[kBN];
                 tmem_ld128(tS, sv);
+                if constexpr (C::kSepP) {
+                    // S_t(j) is read: the MMA warp may compute S_t(j+1) over it now
+                    if (j + 1 < n_kv) {
+                        tc_fence_before();
+                        mbar_arrive(bar(BB::kSFree + t));
+                    }
+                }
                 const float mx = need_mask ? row_max(sv, scale, lim) : row_max_full(sv, scale);
                 // Lazy correction: a row moves its reference only when its max grew by more
                 // than 2^8 over it; O and l are rescaled together, so the result is exact.
@@ -1145,9 +1240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_new = want ? mx : m_ref;
                 const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
 
+                if constexpr (C::kSepP) {
+                    // P_t(j) is written over P_t(j-1): the PV product reading it must be done
+                    if (j > 0) {
+                        if (!wait_all(bar(BB::kOReady + t * 2 + b), ((pv_par >> b) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                }
                 // P = exp2(S * scale - m_ref) as fp16, written over the first 64 columns of S
-                const float rs = need_mask ? exp_pack<KIND>(sv, scale, neg_m, lim, tS)
-                                           : exp_pack_full<KIND>(sv, scale, neg_m, tS);
+                // (or into P_t's own columns)
+                const float rs = need_mask ? exp_pack<KIND>(sv, scale, neg_m, lim, tP)
+                                           : exp_pack_full<KIND>(sv, scale, neg_m, tP);
                 // O holds the PV products of earlier tiles; rescale it (after the last of
                 // them is done) before this tile's P is released to the MMA warp. The warp
                 // does it together when any of its rows needs it (tcgen05.ld/st are
