@@ -1350,13 +1350,14 @@ bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N)
 }
 
 // Heads per block of the unit order: keep the K/V of the heads in flight within about
-// 24 MB of L2, so the query-tile pairs of one head reuse its K/V from L2. G consecutive
-// query heads share one K/V head. (Measured on GB300 against 48 MB, three alternating runs:
-// prefill 1259 -> 1301 TFLOP/s, bf16 prefill +3.4 %, chunked prefill -0.5 %, long within noise.)
+// 16 MB of L2, so the query-tile pairs of one head reuse its K/V from L2. G consecutive
+// query heads share one K/V head. (Measured on GB300, three alternating runs each, prefill in
+// TFLOP/s: 48 MB 1259, 24 MB 1301, 16 MB 1311-1322, 12 MB 1289-1295; at 16 MB the bf16 prefill,
+// grouped-query and chunked prefill are also the fastest of these.)
 int head_block_for(int BH, int Nk, int D, int G)
 {
     const long long kv_head = 4LL * Nk * D; // K and V of one key/value head, fp16
-    const long long hblk = (24LL << 20) / (kv_head > 0 ? kv_head : 1) * G;
+    const long long hblk = (16LL << 20) / (kv_head > 0 ? kv_head : 1) * G;
     return static_cast<int>(hblk < 1 ? 1 : (hblk > BH ? BH : hblk));
 }
 
