@@ -1098,21 +1098,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t tO = lane_base + C::tmem_o(t, pe.b);
             const float inv = pe.l > 0.f ? 1.f / pe.l : 0.f;
+            // Each thread writes its own row, so a warp's store touches 32 rows: 32-byte stores
+            // (when the output is 32-byte aligned; rows are multiples of 32 bytes) fill whole
+            // sectors and take half the sector requests of 16-byte ones.
+            auto store_f32 = [&](float *dst, const uint32_t (&ov)[32], bool v8) {
+                if (v8) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        st_global_v8(dst + e, __float_as_uint(__uint_as_float(ov[e]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 3]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 4]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 5]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 6]) * inv),
+                                     __float_as_uint(__uint_as_float(ov[e + 7]) * inv));
+                } else {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        d4[e >> 2] = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                                 __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+                }
+            };
             if constexpr (SPLIT) {
                 // The range's O / l in fp32 and its logsumexp, for the merge.
                 const size_t r = static_cast<size_t>(pe.split) * args.p.B * args.p.H * p.N +
                                  static_cast<size_t>(pe.bh) * p.N + pe.row;
-                float4 *orow = reinterpret_cast<float4 *>(args.opart + r * D);
+                float *orow = args.opart + r * D;
+                const bool v8 = (reinterpret_cast<uintptr_t>(args.opart) & 31u) == 0;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t ov[32];
                     tmem_ld32(tO + c0, ov);
-                    if (pe.row < p.N) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            orow[(c0 + e) >> 2] = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                                                              __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
-                    }
+                    if (pe.row < p.N)
+                        store_f32(orow + c0, ov, v8);
                 }
                 tc_fence_before();
                 mbar_arrive(bar(BB::kOEmpty + t * 2 + pe.b));
@@ -1122,18 +1142,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if constexpr (TF32) {
                 // fp32 output: O / l as it is
-                float4 *orow = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) +
-                                                          (static_cast<size_t>(pe.bh) * p.N + pe.row) * D);
+                float *orow = reinterpret_cast<float *>(p.o) + (static_cast<size_t>(pe.bh) * p.N + pe.row) * D;
+                const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t ov[32];
                     tmem_ld32(tO + c0, ov);
-                    if (pe.row < p.N) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            orow[(c0 + e) >> 2] = make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                                                              __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
-                    }
+                    if (pe.row < p.N)
+                        store_f32(orow + c0, ov, v8);
                 }
                 tc_fence_before();
                 mbar_arrive(bar(BB::kOEmpty + t * 2 + pe.b));
@@ -1143,6 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             }
             __half *orow = p.o + (static_cast<size_t>(pe.bh) * p.N + pe.row) * D;
+            const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
             constexpr int kChunk = D < 64 ? D : 64; // O columns per TMEM load
 #pragma unroll
             for (int half = 0; half < D / kChunk; ++half) {
@@ -1156,10 +1173,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < kChunk; e += 2)
                     h[e >> 1] = pack2<KIND == kKindBF16>(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
                 if (pe.row < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
+                    if (v8) {
 #pragma unroll
-                    for (int c = 0; c < kChunk / 8; ++c)
-                        dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                        for (int c = 0; c < kChunk / 16; ++c)
+                            st_global_v8(orow + half * kChunk + c * 16, h[8 * c], h[8 * c + 1], h[8 * c + 2],
+                                         h[8 * c + 3], h[8 * c + 4], h[8 * c + 5], h[8 * c + 6], h[8 * c + 7]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + half * kChunk);
+#pragma unroll
+                        for (int c = 0; c < kChunk / 8; ++c)
+                            dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    }
                 }
             }
             tc_fence_before();
