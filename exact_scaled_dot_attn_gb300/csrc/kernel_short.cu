@@ -611,13 +611,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ++k;
                 if (row < N) {
                     const float inv = 1.f / l;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + (head_row0 + row) * D);
+                    uint32_t h[D / 2];
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c)
-                        dst[c] = make_uint4(pack_f16x2(__uint_as_float(ov[8 * c]) * inv, __uint_as_float(ov[8 * c + 1]) * inv),
-                                            pack_f16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv),
-                                            pack_f16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
-                                            pack_f16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
+                    for (int e = 0; e < D; e += 2)
+                        h[e >> 1] = pack_f16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+                    __half *orow = p.o + (head_row0 + row) * D;
+                    if ((reinterpret_cast<uintptr_t>(p.o) & 31u) == 0) {
+                        // whole 32-byte sectors per thread (each thread writes its own row)
+#pragma unroll
+                        for (int c = 0; c < D / 16; ++c)
+                            st_global_v8(orow + 16 * c, h[8 * c], h[8 * c + 1], h[8 * c + 2], h[8 * c + 3],
+                                         h[8 * c + 4], h[8 * c + 5], h[8 * c + 6], h[8 * c + 7]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c)
+                            dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    }
                     if (p.lse)
                         p.lse[head_row0 + row] = (m + log2f(l)) * kLn2;
                 }
