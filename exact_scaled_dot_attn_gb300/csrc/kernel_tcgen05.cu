@@ -175,6 +175,10 @@ struct TcArgs {
     float *opart;   // split-KV partial outputs: [split][B*H*N][D] fp32, O / l of the range
     float *lpart;   // split-KV partial logsumexp: [split][B*H*N] fp32 (-inf: no key in the range)
     unsigned int *status;
+    // 1: one CTA per unit in the unit order; a running CTA takes over the units of CTAs that
+    // have not started (cluster launch control), so the CTAs that finish first take more
+    // units. 0: a persistent grid walks the schedule table.
+    int dynamic;
 };
 
 struct Unit {
@@ -297,9 +301,15 @@ struct UnitStream {
     UnitCursor cur;
     bool has;
     Unit next;
+    uint32_t k; // dynamic schedule: units taken from the shared ring
 };
 __device__ __forceinline__ void stream_init(UnitStream &st, const TcArgs &a, const SchedTable &s)
 {
+    st.k = 0;
+    if (a.dynamic) {
+        st.has = true; // every unit, the first included, comes from the ring
+        return;
+    }
     st.cur = first_unit(s);
     int u;
     st.has = next_unit(a, s, st.cur, u);
@@ -335,8 +345,19 @@ template <int D, int ES = 2> struct Bars {
     static constexpr int kVTEmpty = kVTFull + 2;  // [2]
     // separate P only: the softmax of tile t has read S_t (the next S_t may be written)
     static constexpr int kSFree = kVTEmpty + 2;   // [2]
-    static constexpr int kCount = kSFree + 2;
+    // dynamic schedule: the ring of decoded units (producer -> other roles) and the answer of
+    // the cluster launch control request in flight
+    static constexpr int kUnitFull = kSFree + 2;  // [kUnitSlots]
+    static constexpr int kUnitEmpty = kUnitFull + 4;
+    static constexpr int kClc = kUnitEmpty + 4;
+    static constexpr int kCount = kClc + 1;
+    // byte offsets from the start of the barrier block (which has 1 KB)
+    static constexpr int kClcResp = 640;  // 16-byte answer
+    static constexpr int kUnitRing = 656; // kUnitSlots units
+    static_assert(8 * kCount + 8 <= kClcResp, "barrier block overflow");
 };
+constexpr int kUnitSlots = 4;
+static_assert(Bars<128>::kUnitRing + kUnitSlots * static_cast<int>(sizeof(Unit)) <= 1024, "unit ring overflow");
 
 // Column chunks of the S row: the allowed columns of a row are a prefix e < lim (key
 // padding and the causal diagonal both cut a row at one column), so every 32-column chunk
@@ -595,6 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * BB::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t sClcResp = sBar + BB::kClcResp;
+    Unit *unit_ring = reinterpret_cast<Unit *>(smem + C::kOffBar + BB::kUnitRing);
+    // warps that take units from the ring: the MMA warp, the softmax warps, the transposers
+    constexpr int kRingReaders = 1 + 8 + (TF32 ? 2 : 0);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -625,6 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(BB::kOEmpty + i), kBM);
         }
         mbar_init(bar(BB::kMmaDone), 1);
+        for (int i = 0; i < kUnitSlots; ++i) {
+            mbar_init(bar(BB::kUnitFull + i), 1);
+            mbar_init(bar(BB::kUnitEmpty + i), kRingReaders);
+        }
+        mbar_init(bar(BB::kClc), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(BB::kVReady + i), 1);
             mbar_init(bar(BB::kVTFull + i), 64); // the 64 threads of the transposer warps
@@ -660,6 +690,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
         return r;
     };
+    // The next unit of this CTA, for the roles other than the producer (whole warps). Static
+    // schedule: from the table. Dynamic: from the producer's ring, in order; a unit with
+    // n_kv < 0 marks the end.
+    auto take = [&](UnitStream &st, Unit &U) -> bool {
+        if (!args.dynamic)
+            return stream_take(st, args, sched, U);
+        if (!st.has)
+            return false;
+        const uint32_t slot = st.k % kUnitSlots;
+        if (!warp_wait(bar(BB::kUnitFull + slot), (st.k / kUnitSlots) & 1u)) {
+            st.has = false;
+            return false;
+        }
+        U = unit_ring[slot];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar(BB::kUnitEmpty + slot));
+        ++st.k;
+        if (U.n_kv < 0) {
+            st.has = false;
+            return false;
+        }
+        return true;
+    };
 
     // The producer and MMA roles run on whole warps (converged control flow, warp-uniform
     // operands); one elected lane issues each TMA copy, tcgen05.mma and commit.
@@ -671,12 +725,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         UnitStream us;
         stream_init(us, args, sched);
         Unit U;
-        while (ok && stream_take(us, args, sched, U)) {
+        // Dynamic schedule: the producer decodes every unit of the CTA once and hands it to the
+        // other roles through the ring. Its first unit is the CTA's own; each later one is the
+        // unit of a CTA whose launch a cluster launch control request cancelled. One request
+        // is in flight at a time, made as a unit is published and answered by the time that
+        // unit's loads are issued; after an answer that cancelled nothing none is made.
+        uint32_t pub = 0;           // units published
+        uint32_t clc_par = 0;       // phase parity of the next answer
+        bool clc_pending = false;   // a request is in flight
+        int next_cta = blockIdx.x;  // the CTA whose unit comes next (-1: none)
+        auto publish = [&](const Unit &X) -> bool {
+            const uint32_t slot = pub % kUnitSlots;
+            if (!warp_wait(bar(BB::kUnitEmpty + slot), ((pub / kUnitSlots) & 1u) ^ 1u))
+                return false;
+            if (lane == 0) {
+                unit_ring[slot] = X;
+                mbar_arrive(bar(BB::kUnitFull + slot)); // releases the unit's write
+            }
+            __syncwarp();
+            ++pub;
+            return true;
+        };
+        auto next = [&](Unit &X) -> bool {
+            if (!args.dynamic)
+                return stream_take(us, args, sched, X);
+            if (next_cta < 0)
+                return false;
+            // (the CTA ids map to units through the host's order when it built one)
+            X = decode_unit(args, sched.use ? static_cast<int>(sched.unit[next_cta]) : next_cta);
+            if (!publish(X)) {
+                ok = false;
+                return false;
+            }
+            if (elect_one()) {
+                // the last answer was read (generic proxy) before the request rewrites it
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                mbar_arrive_expect_tx(bar(BB::kClc), 16);
+                clc_try_cancel(sClcResp, bar(BB::kClc));
+            }
+            __syncwarp();
+            clc_pending = true;
+            return true;
+        };
+        auto answer = [&]() -> bool {
+            if (!warp_wait(bar(BB::kClc), clc_par))
+                return false;
+            clc_par ^= 1u;
+            clc_pending = false;
+            const uint64_t *r = reinterpret_cast<const uint64_t *>(smem + C::kOffBar + BB::kClcResp);
+            next_cta = clc_cancelled_x(r[0], r[1]);
+            return true;
+        };
+        while (ok && next(U)) {
+            if (args.dynamic && U.n_kv == 0) {
+                if (!answer())
+                    ok = false;
+                continue;
+            }
             if (U.n_kv == 0)
                 continue;
             const uint32_t qs = q_it % C::kQStages;
-            if (!warp_wait(bar(BB::kQEmpty + qs), ((q_it / C::kQStages) & 1u) ^ 1u))
+            if (!warp_wait(bar(BB::kQEmpty + qs), ((q_it / C::kQStages) & 1u) ^ 1u)) {
+                ok = false;
                 break;
+            }
             ++q_it;
             if (elect_one()) {
                 mbar_arrive_expect_tx(bar(BB::kQFull + qs), 2 * C::kTileBytes);
@@ -709,6 +821,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++kv_it;
                 }
             }
+            if (args.dynamic && ok && !answer())
+                ok = false;
+        }
+        if (args.dynamic) {
+            if (ok) {
+                Unit E = {};
+                E.n_kv = -1; // the end of the CTA's units
+                publish(E);
+            }
+            // (after an abort) the answer in flight lands before the CTA may leave
+            if (clc_pending && lane == 0)
+                mbar_wait(bar(BB::kClc), clc_par, nullptr, kWaitLimitNs);
+            __syncwarp();
         }
         // Loads still in flight land before the CTA may leave (after an abort): wait,
         // bounded by time only, for the latest phase of every slot that was filled.
@@ -795,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         stream_init(us, args, sched);
         // The next unit that has work (units without an allowed key need no MMA).
         auto take_work = [&](Unit &X) -> bool {
-            while (stream_take(us, args, sched, X))
+            while (take(us, X))
                 if (X.n_kv > 0)
                     return true;
             return false;
@@ -834,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sf_par = 0; // bit t: parity of the SFree waits of tile t
             while (ok && have) {
                 const uint32_t uq_slot = q_slot;
-                const bool have_next = take_work(Un);
+                bool have_next = false;
                 for (int j = 0; j < U.n_kv && ok; ++j) {
                     const uint32_t v_pos = kv_it;
                     const uint32_t v_slot = v_pos % C::kStages;
@@ -893,8 +1018,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
-                    if (!has_next && have_next) {
-                        if (!start_unit(Un))
+                    if (!has_next) {
+                        // The next unit is taken only now (the dynamic schedule's producer
+                        // publishes it once this unit's loads are all issued).
+                        have_next = take_work(Un);
+                        if (have_next && !start_unit(Un))
                             break;
                     }
                 }
@@ -906,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok && have) {
             const uint32_t uq_slot = q_slot; // this unit's Q buffer
             ob = C::kOBufs == 2 ? u_par : 0u;
-            const bool have_next = take_work(Un);
+            bool have_next = false;
             // step j: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T; a tile whose
             // causal range ends earlier drops out of the later steps. After the last
             // step the next unit's first S products follow at once, so the softmax
@@ -980,8 +1108,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 ++vt_it;
-                if (!has_next && have_next) {
-                    if (!start_unit(Un))
+                if (!has_next) {
+                    // The next unit is taken only now (the dynamic schedule's producer
+                    // publishes it once this unit's loads are all issued).
+                    have_next = take_work(Un);
+                    if (have_next && !start_unit(Un))
                         break;
                 }
             }
@@ -1014,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             UnitStream us;
             stream_init(us, args, sched);
             Unit U;
-            while (ok && stream_take(us, args, sched, U)) {
+            while (ok && take(us, U)) {
                 for (int j = 0; j < U.n_kv; ++j) {
                     const uint32_t vt = g & 1u, use = g >> 1;
                     if (!warp_wait(bar(BB::kVReady + vt), use & 1u) ||
@@ -1196,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         UnitStream us;
         stream_init(us, args, sched);
         Unit U;
-        while (ok && stream_take(us, args, sched, U)) {
+        while (ok && take(us, U)) {
             const int n_kv = kv_tiles(U, t);
             if (n_kv == 0) {
                 // Nothing to accumulate: rows with no allowed key get O = 0 and lse = -inf
@@ -1412,6 +1543,9 @@ int uniform_pair_tiles(int N, int Nk, int causal)
 // heads over 8): balanced runs were faster at 108 tiles per SM (188 vs 209 us) and slower at
 // 27-47 (70 vs 67 us), which puts it between 5 and 20.
 constexpr long long kUnitCostTiles = 8;
+// Units per SM from which the dynamic schedule is used (measured: 256 units on 152 SMs ran 1 %
+// slower dealt dynamically than by the static table; 1024 to 4096 units ran 1-4 % faster).
+constexpr int kDynamicUnitsPerSm = 3;
 long long balanced_makespan(long long pairs, int nf, int G)
 {
     const long long T = pairs * nf;
@@ -1560,6 +1694,59 @@ void build_balanced_schedule(SchedTable &t, long long pairs, int nf, int G, int 
     t.off[G] = static_cast<uint16_t>(k);
 }
 
+// Order of the units for the dynamic schedule: CTA id c runs unit unit[c]. The units come in
+// the device's unit order (head block by head block, heaviest pair first inside a block), except
+// that the last ~30 % of the work, from a head-block boundary on, is sorted heaviest first across
+// its blocks. The scheduler hands out CTAs that have not started roughly in id order (measured:
+// ascending, shuffled within ~100 ids), so the launch ends on the lightest units whatever the
+// shuffle; in block order alone a heavy unit of the last block could start last.
+void build_dynamic_order(SchedTable &t, int BH, int N, int Nk, int causal, int head_block, int n_pairs,
+                         int n_splits)
+{
+    const int S = n_splits;
+    const int n_units = BH * n_pairs * S;
+    const int per_block = head_block * n_pairs * S;
+    std::vector<long long> wts(n_units);
+    long long total = 0;
+    for (int u = 0; u < n_units; ++u) {
+        const int blk = u / per_block;
+        const int ws = u - blk * per_block;
+        const int split = ws % S;
+        const int w = ws / S;
+        const int hb = std::min(head_block, BH - blk * head_block);
+        const int pair = n_pairs - 1 - w / hb;
+        const int q0 = pair * 2 * kBM;
+        int e0 = Nk, e1 = Nk;
+        if (causal) {
+            e0 = std::max(0, std::min(Nk, q0 + kBM + Nk - N));
+            e1 = std::max(0, std::min(Nk, q0 + 2 * kBM + Nk - N));
+        }
+        const int f0 = (e0 + kBN - 1) / kBN;
+        const int f1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
+        const int nf = std::max(f0, f1);
+        const int j0 = split * nf / S, j1 = (split + 1) * nf / S;
+        wts[u] = std::max(0, std::min(j1, f0) - j0) + std::max(0, std::min(j1, f1) - j0) + 8;
+        total += wts[u];
+    }
+    int cut = 0;
+    long long acc = 0;
+    for (int u = n_units - 1; u >= 0; --u) {
+        acc += wts[u];
+        if (acc * 10 > total * 3) {
+            cut = u + 1;
+            break;
+        }
+    }
+    cut = cut / per_block * per_block;
+    std::vector<int> order(n_units);
+    for (int u = 0; u < n_units; ++u)
+        order[u] = u;
+    std::stable_sort(order.begin() + cut, order.end(), [&](int a, int b) { return wts[a] > wts[b]; });
+    t.use = 1;
+    for (int c = 0; c < n_units; ++c)
+        t.unit[c] = static_cast<uint16_t>(order[c]);
+}
+
 // Schedules are cached per shape (they depend on B*H, N, Nk, the head block, causal, the
 // split count, the SM count and the balanced run length only).
 std::mutex g_sched_mutex;
@@ -1576,7 +1763,10 @@ std::shared_ptr<SchedTable> schedule_for(int BH, int N, int Nk, int causal, int 
     auto t = std::make_shared<SchedTable>();
     memset(t.get(), 0, sizeof(SchedTable));
     const long long n_units = static_cast<long long>(BH) * n_pairs * n_splits;
-    if (bal_nfull > 0)
+    if (bal_nfull < 0) {
+        if (n_units <= kMaxSchedUnits)
+            build_dynamic_order(*t, BH, N, Nk, causal, head_block, n_pairs, n_splits);
+    } else if (bal_nfull > 0)
         build_balanced_schedule(*t, static_cast<long long>(BH) * n_pairs, bal_nfull, grid, n_splits);
     else if (grid <= kMaxCtas && n_units <= kMaxSchedUnits)
         build_schedule(*t, BH, N, Nk, causal, head_block, n_pairs, n_splits, grid);
@@ -1628,6 +1818,7 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
         return cudaErrorInvalidConfiguration;
     a.bal_chunks = 0;
     a.bal_nfull = 0;
+    a.dynamic = 0;
     int grid = a.n_units < sms ? a.n_units : sms;
     if (SPLIT) {
         const int nf = splitkv_balanced_runs(BH, p.N, p.Nk, p.causal && !p.qrows, sms, n_splits);
@@ -1639,8 +1830,20 @@ cudaError_t launch_d(const FwdParams &p, int n_splits, float *opart, float *lpar
             grid = a.bal_chunks;
         }
     }
-    std::shared_ptr<SchedTable> sched = schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block,
-                                                     a.n_pairs, n_splits, grid, a.bal_nfull);
+    // Without balanced runs and with at least kDynamicUnitsPerSm units per SM, the units are dealt
+    // dynamically: one CTA per unit, CTA c running unit unit[c] of the dynamic order
+    // (build_dynamic_order; the unit order when the table does not fit), running CTAs taking
+    // over the units of CTAs that have not started. Fewer units go to the static largest-first
+    // table, which balances a short list better.
+    std::shared_ptr<SchedTable> sched;
+    if (a.bal_chunks == 0 && a.n_units >= kDynamicUnitsPerSm * sms) {
+        a.dynamic = 1;
+        grid = a.n_units;
+        sched = schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block, a.n_pairs, n_splits, grid, -1);
+    } else {
+        sched = schedule_for(BH, p.N, p.Nk, p.causal && !p.qrows, a.head_block, a.n_pairs, n_splits, grid,
+                             a.bal_nfull);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);

@@ -81,6 +81,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// ------------------------------------------------------------------ cluster launch control
+// Asks the scheduler to cancel the launch of a CTA of this grid that has not started yet. The
+// 16-byte answer is written to shared memory at `resp` (16-byte aligned) and completes 16
+// transaction bytes on the mbarrier `bar`. After an answer that cancelled nothing no further
+// request may be made; before `resp` is rewritten by a new request, the reads of the last
+// answer are ordered before it by fence.proxy.async.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar)
+{
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];\n"
+                 ::"r"(resp), "r"(bar)
+                 : "memory");
+}
+
+// The x index of the CTA an answer (lo, hi: its two 64-bit halves) cancelled, or -1 when it
+// cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(uint64_t lo, uint64_t hi)
+{
+    uint32_t ok, x;
+    asm volatile("{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+                 "mov.b128 r, {%2, %3};\n\t"
+                 "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t"
+                 "mov.u32 %1, 0;\n\t"
+                 "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}\n"
+                 : "=r"(ok), "=r"(x)
+                 : "l"(lo), "l"(hi));
+    return ok ? static_cast<int>(x) : -1;
+}
+
 // One lane of the (converged) warp is elected: the lane that issues a single-thread
 // operation (tcgen05.mma, commit, TMA) while the whole warp runs the role's control flow.
 // Operands computed by the whole warp stay warp-uniform, which keeps the issue of a
