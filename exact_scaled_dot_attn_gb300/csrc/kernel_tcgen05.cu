@@ -1696,10 +1696,11 @@ void build_balanced_schedule(SchedTable &t, long long pairs, int nf, int G, int 
 
 // Order of the units for the dynamic schedule: CTA id c runs unit unit[c]. The units come in
 // the device's unit order (head block by head block, heaviest pair first inside a block), except
-// that the last ~30 % of the work, from a head-block boundary on, is sorted heaviest first across
+// that the last ~20 % of the work, from a head-block boundary on, is sorted heaviest first across
 // its blocks. The scheduler hands out CTAs that have not started roughly in id order (measured:
 // ascending, shuffled within ~100 ids), so the launch ends on the lightest units whatever the
-// shuffle; in block order alone a heavy unit of the last block could start last.
+// shuffle; in block order alone a heavy unit of the last block could start last. (A larger
+// sorted share mixes more head blocks in L2: 50 % measured 1.4 % slower on prefill.)
 void build_dynamic_order(SchedTable &t, int BH, int N, int Nk, int causal, int head_block, int n_pairs,
                          int n_splits)
 {
@@ -1732,7 +1733,7 @@ void build_dynamic_order(SchedTable &t, int BH, int N, int Nk, int causal, int h
     long long acc = 0;
     for (int u = n_units - 1; u >= 0; --u) {
         acc += wts[u];
-        if (acc * 10 > total * 3) {
+        if (acc * 10 > total * 2) {
             cut = u + 1;
             break;
         }
