@@ -1696,8 +1696,8 @@ void build_balanced_schedule(SchedTable &t, long long pairs, int nf, int G, int 
 
 // Order of the units for the dynamic schedule: CTA id c runs unit unit[c]. The units come in
 // the device's unit order (head block by head block, heaviest pair first inside a block), except
-// that the last ~20 % of the work, from a head-block boundary on, is sorted heaviest first across
-// its blocks. The scheduler hands out CTAs that have not started roughly in id order (measured:
+// that the last ~20 % of the work, from a head-block boundary on and over at most three head
+// blocks, is sorted heaviest first across its blocks. The scheduler hands out CTAs that have not started roughly in id order (measured:
 // ascending, shuffled within ~100 ids), so the launch ends on the lightest units whatever the
 // shuffle; in block order alone a heavy unit of the last block could start last. (A larger
 // sorted share mixes more head blocks in L2: 50 % measured 1.4 % slower on prefill.)
@@ -1739,6 +1739,9 @@ void build_dynamic_order(SchedTable &t, int BH, int N, int Nk, int causal, int h
         }
     }
     cut = cut / per_block * per_block;
+    // at most three head blocks (48 MB of K/V) are mixed, so the tail's K/V stays in L2 (six
+    // one-head blocks of the N = 32768 workload, sorted together, read K/V 3x from DRAM)
+    cut = std::max(cut, n_units - 3 * per_block);
     std::vector<int> order(n_units);
     for (int u = 0; u < n_units; ++u)
         order[u] = u;
