@@ -175,9 +175,10 @@ struct TcArgs {
     float *opart;   // split-KV partial outputs: [split][B*H*N][D] fp32, O / l of the range
     float *lpart;   // split-KV partial logsumexp: [split][B*H*N] fp32 (-inf: no key in the range)
     unsigned int *status;
-    // 1: one CTA per unit in the unit order; a running CTA takes over the units of CTAs that
-    // have not started (cluster launch control), so the CTAs that finish first take more
-    // units. 0: a persistent grid walks the schedule table.
+    // 1: one CTA per unit, CTA c running unit unit[c] of the schedule table (unit c when the
+    // table is not used); a running CTA takes over the units of CTAs that have not started
+    // (cluster launch control), so the CTAs that finish first take more units. 0: a persistent
+    // grid walks the table's per-CTA lists.
     int dynamic;
 };
 
@@ -190,10 +191,11 @@ struct Unit {
     int split;      // index of that range
 };
 
-// Static schedule computed on the host: CTA c processes the units
-// unit[off[c] .. off[c+1]) in that order (largest-first assignment to the least
-// loaded CTA, head block by head block). When `use` is 0 the CTAs walk the unit
-// order in a snake instead.
+// Schedule table computed on the host. Static schedule: CTA c processes the units
+// unit[off[c] .. off[c+1]) in that order (largest-first assignment to the least loaded CTA,
+// head block by head block); when `use` is 0 the CTAs walk the unit order in a snake instead.
+// Dynamic schedule (TcArgs::dynamic): CTA id c runs unit unit[c] (off is unused); when `use`
+// is 0, unit c.
 constexpr int kMaxCtas = 256;
 constexpr int kMaxSchedUnits = 4096;
 struct SchedTable {
@@ -1613,22 +1615,15 @@ int splitkv_balanced_auto(int BH, int N, int Nk, int causal, int sms, int max_sp
 
 namespace {
 
-// Largest-first assignment of the units to the least loaded CTA. The units are taken in
-// the device's unit order (head block by head block, heaviest pair first inside a
-// block, the key ranges of a pair next to each other), so every CTA works on the same head
-// block at about the same time. The weight of a unit is its count of (Q tile, K/V tile)
-// steps plus a fixed per-unit cost; key lengths are not known on the host and are taken as Nk.
-void build_schedule(SchedTable &t, int BH, int N, int Nk, int causal, int head_block, int n_pairs,
-                    int n_splits, int grid)
+// Weight of every unit in the device's unit order (head block by head block, heaviest pair first
+// inside a block, the key ranges of a pair next to each other): its count of (Q tile, K/V tile)
+// steps plus kUnitCostTiles, the measured cost of starting a unit; key lengths are not known on
+// the host and are taken as Nk.
+std::vector<long long> unit_weights(int BH, int N, int Nk, int causal, int head_block, int n_pairs, int S)
 {
-    const int S = n_splits;
     const int n_units = BH * n_pairs * S;
     const int per_block = head_block * n_pairs * S;
-    using Slot = std::pair<long long, int>; // (load, cta)
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-    for (int c = 0; c < grid; ++c)
-        heap.push({0, c});
-    std::vector<std::vector<uint16_t>> lists(grid);
+    std::vector<long long> wts(n_units);
     for (int u = 0; u < n_units; ++u) {
         const int blk = u / per_block;
         const int ws = u - blk * per_block;
@@ -1646,14 +1641,31 @@ void build_schedule(SchedTable &t, int BH, int N, int Nk, int causal, int head_b
         const int f1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
         const int nf = std::max(f0, f1);
         const int j0 = split * nf / S, j1 = (split + 1) * nf / S;
-        const int n0 = std::max(0, std::min(j1, f0) - j0);
-        const int n1 = std::max(0, std::min(j1, f1) - j0);
-        // (tile steps, plus the measured cost of starting a unit: about six tile steps)
-        const long long weight = n0 + n1 + 8;
+        wts[u] = std::max(0, std::min(j1, f0) - j0) + std::max(0, std::min(j1, f1) - j0) + kUnitCostTiles;
+    }
+    return wts;
+}
+
+// Largest-first assignment of the units to the least loaded CTA. The units are taken in
+// the device's unit order (head block by head block, heaviest pair first inside a
+// block, the key ranges of a pair next to each other), so every CTA works on the same head
+// block at about the same time. The weight of a unit is its count of (Q tile, K/V tile)
+// steps plus a fixed per-unit cost; key lengths are not known on the host and are taken as Nk.
+void build_schedule(SchedTable &t, int BH, int N, int Nk, int causal, int head_block, int n_pairs,
+                    int n_splits, int grid)
+{
+    const std::vector<long long> wts = unit_weights(BH, N, Nk, causal, head_block, n_pairs, n_splits);
+    const int n_units = static_cast<int>(wts.size());
+    using Slot = std::pair<long long, int>; // (load, cta)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int c = 0; c < grid; ++c)
+        heap.push({0, c});
+    std::vector<std::vector<uint16_t>> lists(grid);
+    for (int u = 0; u < n_units; ++u) {
         Slot sl = heap.top();
         heap.pop();
         lists[sl.second].push_back(static_cast<uint16_t>(u));
-        heap.push({sl.first + weight, sl.second});
+        heap.push({sl.first + wts[u], sl.second});
     }
     t.use = 1;
     int k = 0;
@@ -1695,40 +1707,21 @@ void build_balanced_schedule(SchedTable &t, long long pairs, int nf, int G, int 
 }
 
 // Order of the units for the dynamic schedule: CTA id c runs unit unit[c]. The units come in
-// the device's unit order (head block by head block, heaviest pair first inside a block), except
-// that the last ~20 % of the work, from a head-block boundary on and over at most three head
-// blocks, is sorted heaviest first across its blocks. The scheduler hands out CTAs that have not started roughly in id order (measured:
-// ascending, shuffled within ~100 ids), so the launch ends on the lightest units whatever the
-// shuffle; in block order alone a heavy unit of the last block could start last. (A larger
-// sorted share mixes more head blocks in L2: 50 % measured 1.4 % slower on prefill.)
+// the device's unit order, except that the last ~20 % of the work, from a head-block boundary
+// on and over at most three head blocks, is sorted heaviest first across its blocks. The
+// scheduler hands out CTAs that have not started roughly in id order (measured: ascending,
+// shuffled within ~100 ids), so the launch ends on the lightest units whatever the shuffle; in
+// block order alone a heavy unit of the last block could start last. (A larger sorted share
+// mixes more head blocks in L2: 50 % measured 1.4 % slower on prefill.)
 void build_dynamic_order(SchedTable &t, int BH, int N, int Nk, int causal, int head_block, int n_pairs,
                          int n_splits)
 {
-    const int S = n_splits;
-    const int n_units = BH * n_pairs * S;
-    const int per_block = head_block * n_pairs * S;
-    std::vector<long long> wts(n_units);
+    const std::vector<long long> wts = unit_weights(BH, N, Nk, causal, head_block, n_pairs, n_splits);
+    const int n_units = static_cast<int>(wts.size());
+    const int per_block = head_block * n_pairs * n_splits;
     long long total = 0;
-    for (int u = 0; u < n_units; ++u) {
-        const int blk = u / per_block;
-        const int ws = u - blk * per_block;
-        const int split = ws % S;
-        const int w = ws / S;
-        const int hb = std::min(head_block, BH - blk * head_block);
-        const int pair = n_pairs - 1 - w / hb;
-        const int q0 = pair * 2 * kBM;
-        int e0 = Nk, e1 = Nk;
-        if (causal) {
-            e0 = std::max(0, std::min(Nk, q0 + kBM + Nk - N));
-            e1 = std::max(0, std::min(Nk, q0 + 2 * kBM + Nk - N));
-        }
-        const int f0 = (e0 + kBN - 1) / kBN;
-        const int f1 = q0 + kBM < N ? (e1 + kBN - 1) / kBN : 0;
-        const int nf = std::max(f0, f1);
-        const int j0 = split * nf / S, j1 = (split + 1) * nf / S;
-        wts[u] = std::max(0, std::min(j1, f0) - j0) + std::max(0, std::min(j1, f1) - j0) + 8;
-        total += wts[u];
-    }
+    for (long long w : wts)
+        total += w;
     int cut = 0;
     long long acc = 0;
     for (int u = n_units - 1; u >= 0; --u) {
