@@ -4,11 +4,13 @@
 // Engine from Scratch" ("Online Softmax Formulation", "CUDA Kernel Structure"),
 // laid out for the Blackwell tensor core:
 //
-//   work unit   (batch*head, pair of 128-row Q tiles); a persistent grid of one CTA
-//               per SM walks the units in a static order: heads are taken in blocks
-//               whose K/V fit comfortably in L2, and inside a block the units go
-//               heaviest-first (last query rows first under a causal mask) in a snake
-//               over the CTAs, so causal triangles spread evenly without any counter.
+//   work unit   (batch*head, pair of 128-row Q tiles), in a host-built order: heads are
+//               taken in blocks whose K/V fit comfortably in L2, and inside a block the
+//               units go heaviest-first (last query rows first under a causal mask). With
+//               at least three units per SM the grid has one CTA per unit and running CTAs
+//               take over the units of CTAs that have not started (cluster launch
+//               control), so faster CTAs take more units; otherwise a persistent grid of
+//               one CTA per SM walks host-built largest-first lists.
 //               Cross-attention and grouped-query attention (the README's "natural
 //               extensions"): Q tiles are rows of a query head, K/V tiles come from
 //               its key/value head, and the causal diagonal moves by Nk - N.
@@ -30,9 +32,12 @@
 //               At the end of the unit it divides O by l, rounds to fp16, stores O and
 //               the logsumexp.
 //
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d); P_t is
-// packed fp16 in the first 64 columns of S_t. Every mbarrier wait is bounded; a wait
-// that runs out sets the abort flag and the device status word and the CTA unwinds.
+// TMEM columns: S0 [0,128) S1 [128,256), then the O accumulators from column 256 (O_t of
+// buffer b at 256 + (2b + t) d: one buffer per tile at d = 128 and d = 64, two at d = 32).
+// P_t is packed 16-bit in the first 64 columns of S_t (fp32 P of the tf32 kind fills all 128),
+// except at d = 64 (16-bit), where it has its own columns [384, 448) and [448, 512). Every
+// mbarrier wait is bounded; a wait that runs
+// out sets the abort flag and the device status word and the CTA unwinds.
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
 
