@@ -42,6 +42,7 @@ SIGNATURES = {
     "attn_fwd_debug": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i,
                             ctypes.POINTER(DebugOpts), _vp]),
     "attn_auto_path": (_i, [_i, _i]),
+    "attn_debug_schedule": (_i, [_i, _i, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp]),
     "attn_status_str": (ctypes.c_char_p, [_i]),
     "attn_read_device_status": (_i, [_vp]),
     "attn_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp,

@@ -219,6 +219,12 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
 
 } // namespace
 
+extern "C" int attn_debug_schedule(int BH, int N_q, int N_k, int d, int G, int causal, int sms, int *units,
+                                   int units_cap, int *off, int *n_units, int *head_block)
+{
+    return attn::debug_schedule(BH, N_q, N_k, d, G, causal, sms, units, units_cap, off, n_units, head_block);
+}
+
 extern "C" attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *o,
                                         float *lse, int B, int H, int N, int d, float sm_scale,
                                         int causal, const int32_t *key_lengths, int path,

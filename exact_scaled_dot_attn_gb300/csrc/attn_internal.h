@@ -76,6 +76,15 @@ long long naive_padded_cols(int N);
 // Multiprocessor count of the current device (cached per device).
 cudaError_t device_sm_count(int *out);
 
+// The unit schedule the tiled kernel's host side builds for a launch of BH (batch * query head)
+// problems of N query rows over Nk keys at head dimension D, G query heads per key/value head,
+// on `sms` multiprocessors (one key range per Q-tile pair). Returns 1 for the dynamic schedule
+// (units[c] = unit of CTA id c), 0 for the static table (CTA c's units at units[off[c] ..
+// off[c + 1]); off has sms + 1 entries), -1 for bad arguments or a too small `cap`. n_units and
+// head_block receive the unit count and the heads per L2 block.
+int debug_schedule(int BH, int N, int Nk, int D, int G, int causal, int sms, int *units, int cap, int *off,
+                   int *n_units, int *head_block);
+
 // Status codes the kernels write into the device status word.
 constexpr unsigned int kDevStatusTimeout = 1u;
 

@@ -1981,6 +1981,37 @@ cudaError_t launch_splitkv_t(const FwdParams &p, int n_splits, float *opart, flo
 
 } // namespace
 
+int debug_schedule(int BH, int N, int Nk, int D, int G, int causal, int sms, int *units, int cap, int *off,
+                   int *n_units, int *head_block)
+{
+    if (BH < 1 || N < 1 || Nk < 1 || G < 1 || sms < 1 || sms > kMaxCtas || (D != 32 && D != 64 && D != 128) ||
+        (causal != 0 && causal != 1) || !units || !n_units || !head_block)
+        return -1;
+    const int n_pairs = (N + 2 * kBM - 1) / (2 * kBM);
+    const long long nu = static_cast<long long>(BH) * n_pairs;
+    if (nu > cap || nu > 0x7fffffffLL)
+        return -1;
+    const int hb = head_block_for(BH, Nk, D, G);
+    *n_units = static_cast<int>(nu);
+    *head_block = hb;
+    // the same choice and tables as launch_d (one key range: no balanced split-KV runs)
+    if (nu >= static_cast<long long>(kDynamicUnitsPerSm) * sms) {
+        std::shared_ptr<SchedTable> t = schedule_for(BH, N, Nk, causal, hb, n_pairs, 1, static_cast<int>(nu), -1);
+        for (int c = 0; c < nu; ++c)
+            units[c] = t->use ? static_cast<int>(t->unit[c]) : c;
+        return 1;
+    }
+    if (!off)
+        return -1;
+    const int grid = static_cast<int>(nu < sms ? nu : sms);
+    std::shared_ptr<SchedTable> t = schedule_for(BH, N, Nk, causal, hb, n_pairs, 1, grid, 0);
+    for (int c = 0; c <= grid; ++c)
+        off[c] = t->use ? static_cast<int>(t->off[c]) : 0;
+    for (int i = 0; t->use && i < off[grid]; ++i)
+        units[i] = static_cast<int>(t->unit[i]);
+    return 0;
+}
+
 cudaError_t launch_tcgen05(const FwdParams &p, cudaStream_t stream, unsigned int *status)
 {
     switch (p.dtype) {

@@ -150,6 +150,20 @@ attn_status_t attn_fwd_debug(const void *q, const void *k, const void *v, void *
                              const int32_t *key_lengths, int path, const attn_debug_opts_t *opts,
                              attn_stream_t stream);
 
+/* Test hook: the unit schedule of the tiled kernel for a launch of BH = B * H query-head
+ * problems of N_q rows over N_k keys at head dimension d, G = H / H_kv query heads per key/value
+ * head, on `sms` multiprocessors (1 <= sms <= 256), one key range per Q-tile pair (a unit is a
+ * (batch * head, pair of 128-row Q tiles)). Host computation only: no device is touched.
+ * Returns 1 for the dynamic schedule (one CTA per unit; units[c] is the unit of CTA id c),
+ * 0 for the static table (a persistent grid of min(units, sms) CTAs; CTA c's units, in order,
+ * are units[off[c] .. off[c + 1]), off holding sms + 1 entries; all off zero when the table
+ * does not fit the library's limits and the CTAs walk the unit order instead), or -1 for bad
+ * arguments or units_cap below the unit count. Units are numbered in the kernel's unit order:
+ * head blocks of head_block heads, inside a block the Q-tile pairs from the last one down, the
+ * heads of the block next to each other. The caller owns every buffer. */
+int attn_debug_schedule(int BH, int N_q, int N_k, int d, int G, int causal, int sms, int *units,
+                        int units_cap, int *off, int *n_units, int *head_block);
+
 /*
  * Cross-attention and grouped-query attention (the "natural extensions" named in the
  * "cuda-reranker" README): the forward of attn_fwd_path with separate query and key/value
