@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05", "short", "naive"])
+    ap.add_argument("--path", default="auto", choices=["auto", "warp_mma", "tcgen05", "short", "naive", "splitkv"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short-n", action="store_true")
     ap.add_argument("--no-split-kv", action="store_true")
@@ -307,6 +307,10 @@ def main():
             api.fwd_naive(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld,
                           out=od, workspace=naive_ws)
             return
+        if args.path == "splitkv":
+            # split-KV with the automatic split count (the kernel plus the merge kernel)
+            api.fwd_splitkv(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od)
+            return
         api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, key_lengths=kld, out=od,
                 path=args.path)
 
@@ -350,7 +354,7 @@ def main():
     tq, tk, tv = (to_host(torch, x, w.dtype).pin_memory() for x in (q, k, v))
     tkl = torch.from_numpy(kl) if kl is not None else None
     o_host = torch.empty(q.shape, dtype=tq.dtype, pin_memory=True)
-    e2e_path = "auto" if args.path == "naive" else args.path  # (the host-tensor API is fused only)
+    e2e_path = "auto" if args.path in ("naive", "splitkv") else args.path  # (the host-tensor API is fused only)
     for _ in range(2):
         api.fwd(tq, tk, tv, causal=w.causal, sm_scale=w.sm_scale, key_lengths=tkl, out=o_host,
                 path=e2e_path)
@@ -367,7 +371,7 @@ def main():
     d2h = q.nbytes
 
     # Roofline of the dominant (only) kernel.
-    kernel_name = args.path
+    kernel_name = "tcgen05" if args.path == "splitkv" else args.path
     if args.path == "auto":
         kernel_name = api.auto_path(w.N, w.d) if (w.H_kv, w.N_k) == (w.H, w.N) else "tcgen05"
     avg_launch_ms = statistics.mean(launch_ms)
@@ -384,6 +388,14 @@ def main():
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                     "traffic": traffic_from_profile("naive", w.name), "kernel": "naive (three passes)",
                     "peak_source": f"{peak_src} copy bandwidth", "avg_launch_ms": avg_launch_ms}
+    if args.path == "splitkv":
+        # few query rows over many keys: bound by reading K and V
+        min_bytes = sum(x.nbytes for x in (q, k, v)) + q.nbytes
+        gbs = min_bytes / (avg_launch_ms * 1e-3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": traffic_from_profile("tcgen05_splitkv", w.name), "kernel": "tcgen05 split-KV and merge",
+                    "peak_source": f"{peak_src} copy bandwidth", "avg_launch_ms": avg_launch_ms}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
@@ -392,7 +404,7 @@ def main():
         "config": dict(workload_config(w), path=args.path, kernel=kernel_name),
         "e2e": {"value": weak_scaling_value(world, flops, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": steps * (3 if args.path == "naive" else 1),
+        "gpu_launches": steps * {"naive": 3, "splitkv": 2}.get(args.path, 1),
         "roofline": roofline,
         "clocks": clocks,
     }
