@@ -342,7 +342,7 @@ extern "C" int attn_splitkv_auto_splits_ex(int B, int H, int H_kv, int N_q, int 
         return -1;
     int sms = 0;
     if (attn::device_sm_count(&sms) != cudaSuccess || sms < 1)
-        sms = 148;
+        sms = 152; // GB300's count, for a query made where no device answers
     // the shape the kernels run (query heads of a group packed together, see pack_query_groups)
     Shape sh{B, H, H_kv, N_q, N_k, d, ATTN_DTYPE_F16};
     pack_query_groups(sh, causal);

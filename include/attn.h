@@ -229,7 +229,8 @@ attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void
  * outputs and logsumexps of every range). 0 for invalid sizes or n_splits outside 1..16. */
 size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 
-/* The split count attn_fwd_splitkv uses for n_splits <= 0, for the current device's SM count:
+/* The split count attn_fwd_splitkv uses for n_splits <= 0, for the current device's SM count
+ * (152, GB300's, where no device answers):
  * where every pair has the same key tile count and runs of equal length over all pairs (see
  * attn_fwd_splitkv) finish sooner than any equal split, the most runs that touch one pair;
  * otherwise, without a causal mask the most ranges that still give one (Q tile pair, key range) unit per

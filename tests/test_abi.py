@@ -173,7 +173,7 @@ def test_noalloc_scratch_limit(lib):
 
 def test_noalloc_auto_count_lowered_to_fit(lib):
     """With n_splits <= 0 the no-allocation entry point lowers the automatic count until the
-    partials fit its array: here the automatic count (2 ranges on the 148-SM count assumed
+    partials fit its array: here the automatic count (2 ranges on the 152-SM count assumed
     without a GPU) needs more than the array and one range fits, so the call gets past the
     scratch check (and, with no GPU, fails at the device lookup). Skipped where a GPU is
     present: the call would launch on the fake pointers."""
