@@ -373,7 +373,7 @@ def main():
     # Roofline of the dominant (only) kernel.
     kernel_name = "tcgen05" if args.path == "splitkv" else args.path
     if args.path == "auto":
-        kernel_name = api.auto_path(w.N, w.d) if (w.H_kv, w.N_k) == (w.H, w.N) else "tcgen05"
+        kernel_name = api.auto_path_ex(w.H, w.H_kv, w.N, w.N_k, w.d, w.dtype, w.causal)
     avg_launch_ms = statistics.mean(launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -388,13 +388,15 @@ def main():
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                     "traffic": traffic_from_profile("naive", w.name), "kernel": "naive (three passes)",
                     "peak_source": f"{peak_src} copy bandwidth", "avg_launch_ms": avg_launch_ms}
-    if args.path == "splitkv":
+    if args.path == "splitkv" or kernel_name == "decode":
         # few query rows over many keys: bound by reading K and V
         min_bytes = sum(x.nbytes for x in (q, k, v)) + q.nbytes
         gbs = min_bytes / (avg_launch_ms * 1e-3) / 1e9
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        split = args.path == "splitkv"
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                    "traffic": traffic_from_profile("tcgen05_splitkv", w.name), "kernel": "tcgen05 split-KV and merge",
+                    "traffic": traffic_from_profile("tcgen05_splitkv" if split else "decode", w.name),
+                    "kernel": "tcgen05 split-KV and merge" if split else "decode",
                     "peak_source": f"{peak_src} copy bandwidth", "avg_launch_ms": avg_launch_ms}
 
     line = {
@@ -680,8 +682,8 @@ def naive_lines(torch, api, peaks, peak_src):
 
 
 def decode_line(torch, api, peaks, peak_src, flush, w):
-    """One decoding workload: the tiled kernel alone and split-KV (automatic count), GB/s of Q,
-    K, V read and O written once, single launches after the L2 flush."""
+    """One decoding workload: the automatic path, the tiled kernel alone and split-KV (automatic
+    count), GB/s of Q, K, V read and O written once, single launches after the L2 flush."""
     q, k, v, _ = synth.draw_workload(w)
     qd, kd, vd = (to_device(torch, x, w.dtype) for x in (q, k, v))
     od = torch.empty_like(qd)
@@ -691,26 +693,31 @@ def decode_line(torch, api, peaks, peak_src, flush, w):
     ws = torch.empty(api.splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits), dtype=torch.uint8,
                      device="cuda")
 
-    def plain():
+    def auto():
         api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od)
+
+    def plain():
+        api.fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od, path="tcgen05")
 
     def split():
         api.fwd_splitkv(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=od, n_splits=n_splits,
                         workspace=ws)
 
+    kernel = api.auto_path_ex(w.H, w.H_kv, w.N, w.N_k, w.d, w.dtype, w.causal)
     res = {}
-    for name, fn in (("plain", plain), ("split", split)):
+    for name, fn in (("auto", auto), ("plain", plain), ("split", split)):
         time_launches(torch, fn, 3, flush)
         res[name] = statistics.median(time_launches(torch, fn, 30, flush))
     gbs = {name: nbytes / (ms * 1e-3) / 1e9 for name, ms in res.items()}
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    return {"workload": w.describe(), "value": gbs["split"], "unit": "GB/s", "launch_ms": res["split"],
-            "n_splits": n_splits, "bytes": nbytes, "unsplit_value": gbs["plain"],
-            "unsplit_launch_ms": res["plain"],
-            "kernel": "tcgen05 (query heads of a group packed into one tile)",
-            "roofline": {"bound": "hbm", "achieved": gbs["split"], "peak": hbm, "unit": "GB/s",
-                         "frac": gbs["split"] / hbm, "peak_source": f"{peak_src} copy bandwidth"},
-            "timing": "single launches after the L2 flush; split includes the merge kernel"}
+    return {"workload": w.describe(), "value": gbs["auto"], "unit": "GB/s", "launch_ms": res["auto"],
+            "kernel": kernel, "bytes": nbytes,
+            "tcgen05_value": gbs["plain"], "tcgen05_launch_ms": res["plain"],
+            "splitkv_value": gbs["split"], "splitkv_launch_ms": res["split"], "n_splits": n_splits,
+            "roofline": {"bound": "hbm", "achieved": gbs["auto"], "peak": hbm, "unit": "GB/s",
+                         "frac": gbs["auto"] / hbm, "peak_source": f"{peak_src} copy bandwidth"},
+            "timing": "single launches after the L2 flush; split-KV includes the merge kernel; "
+                      "tcgen05: query heads of a group packed into one tile"}
 
 if __name__ == "__main__":
     sys.exit(main())

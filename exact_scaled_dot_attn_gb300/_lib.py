@@ -23,8 +23,11 @@ PATH_AUTO = 0
 PATH_WARP_MMA = 1
 PATH_TCGEN05 = 2
 PATH_SHORT = 3
+PATH_DECODE = 4
 PATHS = {"auto": PATH_AUTO, "warp_mma": PATH_WARP_MMA, "tcgen05": PATH_TCGEN05,
-         "short": PATH_SHORT}
+         "short": PATH_SHORT, "decode": PATH_DECODE}
+DECODE_MAX_ROWS = 16     # query rows per head (after query-group packing) the decoding kernel takes
+DECODE_MIN_KEYS = 256    # ATTN_DECODE_MIN_KEYS
 
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 
@@ -42,6 +45,7 @@ SIGNATURES = {
     "attn_fwd_debug": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i,
                             ctypes.POINTER(DebugOpts), _vp]),
     "attn_auto_path": (_i, [_i, _i]),
+    "attn_auto_path_ex": (_i, [_i, _i, _i, _i, _i, _i, _i]),
     "attn_debug_schedule": (_i, [_i, _i, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp]),
     "attn_status_str": (ctypes.c_char_p, [_i]),
     "attn_read_device_status": (_i, [_vp]),

@@ -41,8 +41,9 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = Fal
     key_lengths: int32 [B]; keys j >= key_lengths[b] are excluded.
     sm_scale: defaults to 1/sqrt(d).
     return_lse: also return the fp32 [B, H, N] logsumexp.
-    path: "auto", "warp_mma", "tcgen05" or "short" (kernel choice; see include/attn.h;
-    "short" takes N <= 256 with d in {32, 64}).
+    path: "auto", "warp_mma", "tcgen05", "short" or "decode" (kernel choice; see
+    include/attn.h; "short" takes N <= 256 with d in {32, 64}; "decode" at most 16 query rows
+    per head, counting the query heads of a group together when H_kv < H).
     Device tensors run asynchronously on the current stream. CPU tensors are
     copied to the current CUDA device and back, and the call returns after the
     copy back has finished.
@@ -329,6 +330,19 @@ def auto_path(N: int, d: int) -> str:
         if c == code and name != "auto":
             return name
     raise ValueError(f"unsupported head dimension {d}")
+
+
+def auto_path_ex(H: int, H_kv: int, N_q: int, N_k: int, d: int, dtype: str = "f16",
+                 causal: bool = False) -> str:
+    """Name of the kernel the "auto" path runs for H query heads over H_kv key/value heads, N_q
+    query rows over N_k keys, head dimension d and element type "f16", "bf16" or "f32"."""
+    dt = {"f16": _lib.DTYPE_F16, "bf16": _lib.DTYPE_BF16, "f32": _lib.DTYPE_F32}[dtype]
+    code = _lib.lib().attn_auto_path_ex(int(H), int(H_kv), int(N_q), int(N_k), int(d), dt,
+                                        int(bool(causal)))
+    for name, c in _lib.PATHS.items():
+        if c == code and name != "auto":
+            return name
+    raise ValueError("unsupported shape or element type")
 
 
 def read_device_status() -> int:

@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
-SOURCES = ["attn_api.cu", "kernel_warp_mma.cu", "kernel_tcgen05.cu", "kernel_short.cu", "kernel_naive.cu", "kernel_f32.cu"]
+SOURCES = ["attn_api.cu", "kernel_warp_mma.cu", "kernel_tcgen05.cu", "kernel_short.cu", "kernel_naive.cu", "kernel_f32.cu",
+           "kernel_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

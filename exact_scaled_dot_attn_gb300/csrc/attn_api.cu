@@ -8,6 +8,8 @@
 #include <cstdint>
 #include <mutex>
 
+extern "C" int attn_auto_path(int N, int d);
+
 namespace {
 
 // Per-device status word written by kernels whose bounded waits run out.
@@ -131,6 +133,22 @@ void pack_query_groups(Shape &sh, int &causal)
     }
 }
 
+// The decoding kernel takes fp16 and bf16 problems of at most kDecodeMaxRows rows per head
+// (counted after packing).
+bool decode_fits(const Shape &sh) { return sh.dtype != ATTN_DTYPE_F32 && sh.Nq <= attn::kDecodeMaxRows; }
+
+// The kernel ATTN_PATH_AUTO runs for a (packed) shape.
+int auto_choice(const Shape &sh)
+{
+    if (decode_fits(sh) && sh.Nk >= ATTN_DECODE_MIN_KEYS)
+        return ATTN_PATH_DECODE; // a few rows over many keys: bound by reading K and V
+    if (sh.dtype == ATTN_DTYPE_F32)
+        return ATTN_PATH_WARP_MMA; // fp32 accuracy
+    if (sh.self() && sh.dtype == ATTN_DTYPE_F16)
+        return attn_auto_path(sh.Nq, sh.d);
+    return ATTN_PATH_TCGEN05;
+}
+
 // One forward pass on the chosen kernel (the automatic choice when path is ATTN_PATH_AUTO).
 attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, const Shape &sh_in,
                       float sm_scale, int causal_in, const int32_t *key_lengths, int path,
@@ -173,7 +191,7 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     if (st != ATTN_OK)
         return st;
     if (path != ATTN_PATH_AUTO && path != ATTN_PATH_WARP_MMA && path != ATTN_PATH_TCGEN05 &&
-        path != ATTN_PATH_SHORT)
+        path != ATTN_PATH_SHORT && path != ATTN_PATH_DECODE)
         return ATTN_ERR_UNSUPPORTED;
     // an explicitly chosen short-sequence kernel takes only the shapes the caller gave it
     if (path == ATTN_PATH_SHORT && !sh_in.self())
@@ -185,18 +203,17 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
     // tiled tcgen05 kernel only.
     if (path == ATTN_PATH_SHORT && (!sh.self() || sh.Nq > 256 || sh.d > 64))
         return ATTN_ERR_UNSUPPORTED;
-    // bf16 runs on the tcgen05 kernel only; fp32 on the tcgen05 kernel (TF32 products) or on the
-    // warp-level kernel (split-TF32 products, fp32 accuracy)
-    if (sh.dtype == ATTN_DTYPE_BF16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05)
+    if (path == ATTN_PATH_DECODE && !decode_fits(sh))
+        return ATTN_ERR_UNSUPPORTED;
+    // bf16 runs on the tcgen05 and decoding kernels only; fp32 on the tcgen05 kernel (TF32
+    // products) or on the warp-level kernel (split-TF32 products, fp32 accuracy)
+    if (sh.dtype == ATTN_DTYPE_BF16 && path != ATTN_PATH_AUTO && path != ATTN_PATH_TCGEN05 &&
+        path != ATTN_PATH_DECODE)
         return ATTN_ERR_UNSUPPORTED;
     if (sh.dtype == ATTN_DTYPE_F32 && path == ATTN_PATH_SHORT)
         return ATTN_ERR_UNSUPPORTED;
-    if (path == ATTN_PATH_AUTO) {
-        if (sh.dtype == ATTN_DTYPE_F32)
-            path = ATTN_PATH_WARP_MMA; // fp32 accuracy
-        else
-            path = (sh.self() && sh.dtype == ATTN_DTYPE_F16) ? attn_auto_path(sh.Nq, sh.d) : ATTN_PATH_TCGEN05;
-    }
+    if (path == ATTN_PATH_AUTO)
+        path = auto_choice(sh);
 
     attn::FwdParams p = make_params(q, k, v, o, lse, sh, sm_scale, causal, key_lengths);
     if (opts && opts->wait_limit_ns)
@@ -205,7 +222,9 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
-    if (path == ATTN_PATH_TCGEN05 || path == ATTN_PATH_SHORT) {
+    if (path == ATTN_PATH_DECODE) {
+        err = attn::launch_decode(p, s);
+    } else if (path == ATTN_PATH_TCGEN05 || path == ATTN_PATH_SHORT) {
         unsigned int *status = nullptr;
         err = status_word(&status);
         if (err == cudaSuccess)
@@ -218,6 +237,17 @@ attn_status_t run_fwd(const void *q, const void *k, const void *v, void *o, floa
 }
 
 } // namespace
+
+extern "C" int attn_auto_path_ex(int H, int H_kv, int N_q, int N_k, int d, int dtype, int causal)
+{
+    if (H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_k < 1 || (d != 32 && d != 64 && d != 128) ||
+        (dtype != ATTN_DTYPE_F16 && dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_F32) ||
+        (dtype == ATTN_DTYPE_F32 && d != 32) || (causal != 0 && causal != 1))
+        return -1;
+    Shape sh{1, H, H_kv, N_q, N_k, d, dtype};
+    pack_query_groups(sh, causal);
+    return auto_choice(sh);
+}
 
 extern "C" int attn_debug_schedule(int BH, int N_q, int N_k, int d, int G, int causal, int sms, int *units,
                                    int units_cap, int *off, int *n_units, int *head_block)

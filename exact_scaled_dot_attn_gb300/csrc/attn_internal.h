@@ -73,6 +73,13 @@ cudaError_t launch_f32(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_naive(const FwdParams &p, float *s, __half *pm, cudaStream_t stream);
 long long naive_padded_cols(int N);
 
+// Decoding kernel (CUDA cores, no tensor cores): at most kDecodeMaxRows query rows per head
+// (after query-group packing), fp16 or bf16, d in {32, 64, 128}, any key count. One
+// thread-block cluster per head streams the head's keys and merges through distributed shared
+// memory.
+constexpr int kDecodeMaxRows = 16;
+cudaError_t launch_decode(const FwdParams &p, cudaStream_t stream);
+
 // Multiprocessor count of the current device (cached per device).
 cudaError_t device_sm_count(int *out);
 

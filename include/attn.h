@@ -94,17 +94,26 @@ typedef enum {
     ATTN_DTYPE_F32 = 2
 } attn_dtype_t;
 
-/* Which kernel runs the forward. AUTO runs the short-sequence kernel for d = 32 with
- * N <= 256 and the tiled tcgen05 kernel everywhere else (the fastest at every measured
+/* Which kernel runs the forward. AUTO runs the decoding kernel for problems of at most 16
+ * query rows per head (after the query-group packing of attn_fwd_ex) over at least
+ * ATTN_DECODE_MIN_KEYS keys in fp16 or bf16, the short-sequence kernel for d = 32 with
+ * N <= 256, and the tiled tcgen05 kernel everywhere else (the fastest at every measured
  * shape); the other kernels remain selectable explicitly. */
 typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_WARP_MMA = 1, /* warp-level mma.sync tile kernel: every d, every N */
     ATTN_PATH_TCGEN05 = 2,  /* TMA + tcgen05/TMEM warp-specialised tiled kernel: every d, every N */
-    ATTN_PATH_SHORT = 3     /* tcgen05 kernel holding a Q tile's whole score row in TMEM
+    ATTN_PATH_SHORT = 3,    /* tcgen05 kernel holding a Q tile's whole score row in TMEM
                                (two CTAs per SM, heads dealt longest first): N <= 256,
                                d in {32, 64} */
+    ATTN_PATH_DECODE = 4    /* decoding kernel on the CUDA cores, K and V streamed once through
+                               shared memory by thread-block clusters that merge a head's key
+                               ranges in distributed shared memory: at most 16 query rows per
+                               head (counted after query-group packing), fp16 or bf16, any N_k */
 } attn_path_t;
+
+/* Fewest keys for which ATTN_PATH_AUTO takes the decoding kernel. */
+#define ATTN_DECODE_MIN_KEYS 256
 
 /*
  * Forward without logsumexp. Arguments as described above:
@@ -181,10 +190,13 @@ int attn_debug_schedule(int BH, int N_q, int N_k, int d, int G, int causal, int 
  *   dtype        attn_dtype_t of q, k, v and o (all four the same): ATTN_DTYPE_F16, or
  *                ATTN_DTYPE_BF16 (tcgen05 kernel only), or ATTN_DTYPE_F32 (d = 32 only; see
  *                attn_dtype_t for its two paths); another value or d is ATTN_ERR_UNSUPPORTED
- *   path         ATTN_PATH_AUTO (for fp16 self-attention shapes the kernel attn_auto_path
- *                selects, the fp32-accurate kernel for fp32, the tcgen05 kernel otherwise),
+ *   path         ATTN_PATH_AUTO (the decoding kernel for fp16 and bf16 problems of at most
+ *                16 query rows per head after packing over at least ATTN_DECODE_MIN_KEYS keys;
+ *                else for fp16 self-attention shapes the kernel attn_auto_path selects, the
+ *                fp32-accurate kernel for fp32, the tcgen05 kernel otherwise),
  *                ATTN_PATH_TCGEN05 or ATTN_PATH_WARP_MMA (fp16 and fp32); ATTN_PATH_SHORT
- *                takes fp16 self-attention shapes only (H_kv = H, N_q = N_k); any other
+ *                takes fp16 self-attention shapes only (H_kv = H, N_q = N_k); ATTN_PATH_DECODE
+ *                fp16 and bf16 with at most 16 query rows per head after packing; any other
  *                combination is ATTN_ERR_UNSUPPORTED.
  * B, H, H_kv, N_q, N_k >= 1 (else ATTN_ERR_INVALID_ARG, as is H not a multiple of H_kv); the
  * element count of every tensor must fit int64 and B*H int32. The other arguments, layouts
@@ -326,6 +338,12 @@ size_t attn_noalloc_scratch_bytes(void);
 /* The kernel ATTN_PATH_AUTO selects for sequence length N and head dimension d
  * (an attn_path_t value), or -1 when d is unsupported. No CUDA call is made. */
 int attn_auto_path(int N, int d);
+
+/* The kernel ATTN_PATH_AUTO selects in attn_fwd_ex for H query heads over H_kv key/value heads,
+ * N_q query rows over N_k keys, head dimension d, element type dtype (attn_dtype_t) and the
+ * causal flag (an attn_path_t value), or -1 for invalid or unsupported arguments. The batch
+ * size and key lengths do not enter the choice. No CUDA call is made. */
+int attn_auto_path_ex(int H, int H_kv, int N_q, int N_k, int d, int dtype, int causal);
 
 /* Static description of a status code. Never NULL. */
 const char *attn_status_str(attn_status_t status);

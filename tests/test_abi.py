@@ -211,6 +211,10 @@ def call_ex(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=4, Hkv=2, Nq=8, Nk=32, d=6
     (dict(dtype=-1), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=_lib.DTYPE_BF16, path=_lib.PATH_WARP_MMA), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=_lib.DTYPE_BF16, Hkv=4, Nk=8, d=32, path=_lib.PATH_SHORT), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(H=4, Hkv=1, Nq=5, path=_lib.PATH_DECODE), _lib.ATTN_ERR_UNSUPPORTED),   # 20 packed rows
+    (dict(H=4, Hkv=4, Nq=17, path=_lib.PATH_DECODE), _lib.ATTN_ERR_UNSUPPORTED),  # 17 rows
+    (dict(dtype=_lib.DTYPE_F32, d=32, Nq=1, path=_lib.PATH_DECODE), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(path=5), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(B=1 << 17, H=1 << 10, Hkv=1 << 10, Nq=8, Nk=1 << 30, d=128), _lib.ATTN_ERR_INVALID_ARG),
 ])
 def test_fwd_ex_validation(lib, kw, expected):

@@ -42,5 +42,5 @@ def test_dtype_codes():
 
 
 def test_path_names_match_the_c_enum():
-    # attn_path_t: AUTO 0, WARP_MMA 1, TCGEN05 2, SHORT 3
-    assert _lib.PATHS == {"auto": 0, "warp_mma": 1, "tcgen05": 2, "short": 3}
+    # attn_path_t: AUTO 0, WARP_MMA 1, TCGEN05 2, SHORT 3, DECODE 4
+    assert _lib.PATHS == {"auto": 0, "warp_mma": 1, "tcgen05": 2, "short": 3, "decode": 4}

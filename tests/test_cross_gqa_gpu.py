@@ -2,7 +2,8 @@
 queries [B, H, N_q, d] over keys and values [B, H_kv, N_k, d], query head h reading key/value
 head h // (H // H_kv), and under the causal mask query i seeing keys j <= i + N_k - N_q.
 
-Every case runs through the C ABI on the tcgen05 and warp-level kernels and on split-KV, and is
+Every case runs through the C ABI on the tcgen05 and warp-level kernels, on the decoding kernel
+where it fits (at most 16 query rows per head after packing), and on split-KV, and is
 compared element by element with the fp64 oracle: query blocks shorter and longer than the key
 sequence (the latter with leading rows that see no key), one query row, ragged lengths, key
 padding, every head dimension and group size 1 (multi-query) to H (multi-head). The two
@@ -63,7 +64,9 @@ def test_cross_gqa_matches_oracle(case):
     B, H, Hkv, Nq, Nk, d, causal, _ = case
     q, k, v, kl = _draw(case, seed=3000 + Nq + Nk + d + Hkv)
     o_ref, lse_ref = oracle_full(q, k, v, causal=causal, key_lengths=kl)
-    for kern in ("tcgen05", "warp_mma"):
+    packed_rows = (H // Hkv) * Nq if (Hkv < H and Nq < 128) else Nq
+    kernels = ("tcgen05", "warp_mma") + (("decode",) if packed_rows <= _lib.DECODE_MAX_ROWS else ())
+    for kern in kernels:
         o, lse = run_gpu(q, k, v, causal=causal, key_lengths=kl, path=kern)
         compare(o, lse, o_ref, lse_ref, what=f"{kern} {_ids(case)}")
     for S in (2, 0):
