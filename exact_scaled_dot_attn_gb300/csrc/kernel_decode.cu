@@ -4,22 +4,20 @@
 // maximum and normaliser of "Self-Attention Kernel & Inference Engine from Scratch", "Online
 // Softmax Formulation"); only the decomposition differs.
 //
-// With at most 16 query rows per head there is almost nothing to contract: the work is reading
-// K and V once, so the kernel is built for HBM, not for the tensor cores. Each head is handled
-// by a thread-block cluster of C CTAs (C = 1, 2, 4 or 8, chosen so the grid fills the SMs). CTA
-// c of the cluster streams its contiguous share of the head's 32-key tiles through shared
-// memory with cp.async (three stages, 16-byte copies, the tail zero-filled), and keeps the
-// running state of every row:
-//   scores    lane = key, warp = quarter of the head dimension; the four partial dot products
-//             of a key meet in shared memory (fp32; Q is held pre-scaled by sm_scale * log2 e)
-//   softmax   warp w takes rows w, w + 4, ...; lane = key: the tile maximum and sum by warp
-//             shuffles, P = 2^(s - m), the rescale factor 2^(m_old - m_new) of the row
-//   P V       warp w takes 8 of the tile's keys, lane = D / 32 columns, all rows; the four
-//             warps' partial outputs are added once at the end
-// The CTAs of a cluster then merge their partial (m, l, O) through distributed shared memory
-// (the two-block merge of the same section, applied to C blocks), each CTA writing its share of
-// the head's output elements. No workspace, no second launch, no waits other than the cluster
-// and CTA barriers.
+// With at most 16 query rows per head the work is reading K and V once: the kernel is built to
+// keep HBM busy. Each head is handled by a thread-block cluster of C CTAs (C = 1, 2, 4 or 8,
+// chosen so the grid fits one wave of resident CTAs). CTA c of the cluster streams its
+// contiguous share of the head's 64-key tiles through shared memory with cp.async (three
+// stages, 16-byte copies, the rows of a tile XOR-swizzled in 16-byte chunks, keys past the end
+// zero-filled). All four warps hold the head's 16 query rows (rows past N are zero) and warp w
+// takes keys 16 w .. 16 w + 15 of every tile, with its own running maximum, normaliser and
+// output: the two products of a tile are warp-level tensor-core instructions (mma.sync m16n8k16,
+// 16-bit inputs, fp32 accumulation; P rounded to the input type), which keeps the instruction
+// count per key far below the time its bytes take to arrive. After the last tile the four warps
+// are merged in shared memory and the CTAs of the cluster merge their (m, l, O) through
+// distributed shared memory (the two-block merge of the same section, applied to 4 C blocks),
+// each CTA writing its share of the head's output elements. No workspace, no second launch,
+// no waits other than the cluster and CTA barriers.
 #include "attn_internal.h"
 
 #include <math.h>
@@ -35,34 +33,38 @@ using warpmma::cp_async16;
 using warpmma::cp_async_commit;
 using warpmma::cp_async_wait;
 using warpmma::ex2;
+using warpmma::ldsm_x4;
+using warpmma::ldsm_x4_t;
+using warpmma::swz;
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kKT = 32;        // keys per tile
+constexpr int kRows = 16;      // query rows per head in every warp (the M of the MMA)
+constexpr int kKT = 64;        // keys per tile; warp w takes keys 16 w .. 16 w + 15
 constexpr int kStages = 3;     // tiles in shared memory (two in flight while one is used)
 constexpr int kMaxCluster = 8; // portable cluster size
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Shared-memory layout of one CTA (byte offsets). K rows are padded by 16 bytes so the 32
-// lanes of a warp reading 32 different rows at the same columns hit distinct banks; V rows are
-// read along the row and need no padding.
-template <int D, int R> struct DecSmem {
-    static constexpr int kKs = D + 8; // K row stride (elements)
-    static constexpr int kVs = D;     // V row stride (elements)
-    static constexpr int kStageElems = kKT * (kKs + kVs);
+// Shared-memory layout of one CTA (byte offsets). K and V tiles are [kKT][D] and Q is [16][D],
+// each row's 16-byte chunks XOR-swizzled by its row index (warpmma::swz) so that the eight
+// rows an ldmatrix phase reads fall into different banks.
+template <int D> struct DecSmem {
+    static constexpr int kTileBytes = kKT * D * 2;      // one K or one V tile
+    static constexpr int kStageBytes = 2 * kTileBytes;  // K, then V
     static constexpr int kKv = 0;
-    static constexpr int kKvBytes = kStages * kStageElems * 2;
-    static constexpr int kQ = kKvBytes;                        // fp32 [R][D]
-    static constexpr int kSp = kQ + R * D * 4;                 // fp32 [kWarps][R][kKT]
-    static constexpr int kPt = kSp + kWarps * R * kKT * 4;     // fp32 [kKT][R]
-    static constexpr int kM = kPt + kKT * R * 4;               // fp32 [R]
-    static constexpr int kL = kM + R * 4;                      // fp32 [R]
-    static constexpr int kAl = kL + R * 4;                     // fp32 [R]
-    static constexpr int kLim = kAl + R * 4;                   // int [R]
-    static constexpr int kBytes = kLim + R * 4;
-    // after the loop the K/V stages hold the warps' partial outputs, fp32 [kWarps][R][D]
-    static_assert(kWarps * R * D * 4 <= kKvBytes, "partial outputs must fit the K/V stages");
-    static_assert(kQ % 16 == 0 && kSp % 16 == 0 && kPt % 16 == 0, "16-byte aligned regions");
+    static constexpr int kKvBytes = kStages * kStageBytes;
+    static constexpr int kQ = kKvBytes;                  // [16][D]
+    static constexpr int kMw = kQ + kRows * D * 2;       // fp32 [kWarps][16] per-warp maxima
+    static constexpr int kLw = kMw + kWarps * kRows * 4; // fp32 [kWarps][16] per-warp sums
+    static constexpr int kM = kLw + kWarps * kRows * 4;  // fp32 [16] the CTA's maxima
+    static constexpr int kL = kM + kRows * 4;            // fp32 [16] the CTA's sums
+    static constexpr int kLim = kL + kRows * 4;          // int [16] key limit of every row
+    static constexpr int kBytes = kLim + kRows * 4;
+    // after the last tile the stages hold the warps' outputs, fp32 [kWarps][16][D], then the
+    // CTA's, fp32 [16][D]
+    static constexpr int kOw = 0;
+    static constexpr int kOb = kWarps * kRows * D * 4;
+    static_assert(kOb + kRows * D * 4 <= kKvBytes, "partial outputs must fit the K/V stages");
 };
 
 struct DecArgs {
@@ -74,22 +76,37 @@ struct DecArgs {
     float scale_log2;
 };
 
-template <typename T> struct Elt;
-template <> struct Elt<__half> {
-    static __device__ __forceinline__ float2 pair(uint32_t w)
+// D[16x8] += A[16x16] * B[16x8] with 16-bit inputs of type T and fp32 accumulators, and the
+// packing of two fp32 values into one A-fragment register of type T.
+template <typename T> struct Mma;
+template <> struct Mma<__half> {
+    static __device__ __forceinline__ void run(float *c, const unsigned *a, unsigned b0, unsigned b1)
     {
-        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+                     "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
-    static __device__ __forceinline__ float one(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ unsigned pack(float lo, float hi)
+    {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<unsigned *>(&h);
+    }
     static __device__ __forceinline__ __half from(float x) { return __float2half_rn(x); }
 };
-template <> struct Elt<__nv_bfloat16> {
-    // a bf16 value is the high half of the fp32 value with the same bits
-    static __device__ __forceinline__ float2 pair(uint32_t w)
+template <> struct Mma<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float *c, const unsigned *a, unsigned b0, unsigned b1)
     {
-        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+                     "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
-    static __device__ __forceinline__ float one(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ unsigned pack(float lo, float hi)
+    {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<unsigned *>(&h);
+    }
     static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
 };
 
@@ -128,53 +145,19 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr, uint32_t rank)
     return x;
 }
 
-__device__ __forceinline__ float warp_max(float x)
+// One head (batch * query head) per cluster; see the file comment. D: head dimension.
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, 2) attn_fwd_decode_kernel(DecArgs a)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
-__device__ __forceinline__ float warp_sum(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// DPL consecutive elements of a shared-memory row as fp32.
-template <typename T, int DPL> __device__ __forceinline__ void load_cols(float *f, const T *p)
-{
-    if constexpr (DPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(p);
-        const float2 a = Elt<T>::pair(w.x), b = Elt<T>::pair(w.y);
-        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    } else if constexpr (DPL == 2) {
-        const float2 a = Elt<T>::pair(*reinterpret_cast<const uint32_t *>(p));
-        f[0] = a.x; f[1] = a.y;
-    } else {
-        f[0] = Elt<T>::one(*p);
-    }
-}
-
-// One head (batch * query head) per cluster; see the file comment. D: head dimension, R: query
-// rows per head rounded up to 4, 8 or 16 (rows >= N are padding and are not written).
-template <int D, int R, typename T>
-__global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kernel(DecArgs a)
-{
-    using L = DecSmem<D, R>;
-    constexpr int DQ = D / kWarps; // head-dimension columns per warp in the score phase
-    constexpr int DPL = D / 32;    // columns per lane in the P V phase
-    constexpr int KPW = kKT / kWarps; // keys per warp in the P V phase
-    extern __shared__ __align__(16) unsigned char smem[];
-    T *kv = reinterpret_cast<T *>(smem + L::kKv);
-    float *qs = reinterpret_cast<float *>(smem + L::kQ);
-    float *sp = reinterpret_cast<float *>(smem + L::kSp);
-    float *pt = reinterpret_cast<float *>(smem + L::kPt);
+    using L = DecSmem<D>;
+    constexpr int CPR = D / 8; // 16-byte chunks per row
+    extern __shared__ __align__(1024) unsigned char smem[];
+    T *kvs = reinterpret_cast<T *>(smem + L::kKv);
+    T *qsm = reinterpret_cast<T *>(smem + L::kQ);
+    float *mw = reinterpret_cast<float *>(smem + L::kMw);
+    float *lw = reinterpret_cast<float *>(smem + L::kLw);
     float *m_s = reinterpret_cast<float *>(smem + L::kM);
     float *l_s = reinterpret_cast<float *>(smem + L::kL);
-    float *al_s = reinterpret_cast<float *>(smem + L::kAl);
     int *lim_s = reinterpret_cast<int *>(smem + L::kLim);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -192,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kern
     int klen = a.Nk;
     if (a.key_lengths)
         klen = min(max(a.key_lengths[b], 0), a.Nk);
-    if (tid < R) {
+    if (tid < kRows) {
         int lim = 0;
         if (tid < a.N) {
             lim = klen;
@@ -204,35 +187,36 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kern
             }
         }
         lim_s[tid] = lim;
-        m_s[tid] = -INFINITY;
-        l_s[tid] = 0.f;
     }
-    for (int e = tid; e < R * D; e += kThreads) {
-        const int r = e / D;
-        qs[e] = r < a.N ? Elt<T>::one(qg[e]) * a.scale_log2 : 0.f;
+    // the head's query rows (rows >= N read as zero): the oldest copy group
+    for (int c = tid; c < kRows * CPR; c += kThreads) {
+        const int r = c / CPR, ch = c % CPR;
+        const bool ok = r < a.N;
+        cp_async16(qsm + swz<D>(r, ch), qg + static_cast<long long>(ok ? r : 0) * D + ch * 8, ok);
     }
+    cp_async_commit();
     __syncthreads();
     int n_keys = 0;
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < kRows; ++r)
         n_keys = max(n_keys, lim_s[r]);
+    const int lim_a = lim_s[lane >> 2], lim_b = lim_s[(lane >> 2) + 8]; // this thread's two rows
     const int n_tiles = (n_keys + kKT - 1) / kKT;
     const int t0 = static_cast<int>(static_cast<long long>(n_tiles) * rank / C);
     const int nt = static_cast<int>(static_cast<long long>(n_tiles) * (rank + 1) / C) - t0;
 
     // tile t of this CTA (keys (t0 + t) * kKT ...) into stage s; keys >= n_keys read as zero
     auto load_tile = [&](int t, int s) {
-        constexpr int CPR = D / 8; // 16-byte chunks per row
-        T *ks = kv + s * L::kStageElems;
-        T *vs = ks + kKT * L::kKs;
+        T *ks = kvs + s * (L::kStageBytes / 2);
+        T *vs = ks + L::kTileBytes / 2;
         const int key0 = (t0 + t) * kKT;
         for (int c = tid; c < kKT * CPR; c += kThreads) {
             const int r = c / CPR, ch = c % CPR;
             const int key = key0 + r;
             const bool ok = key < n_keys;
             const long long src = static_cast<long long>(ok ? key : 0) * D + ch * 8;
-            cp_async16(ks + r * L::kKs + ch * 8, kg + src, ok);
-            cp_async16(vs + r * L::kVs + ch * 8, vg + src, ok);
+            cp_async16(ks + swz<D>(r, ch), kg + src, ok);
+            cp_async16(vs + swz<D>(r, ch), vg + src, ok);
         }
     };
 
@@ -242,13 +226,20 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kern
             load_tile(s, s);
         cp_async_commit();
     }
+    cp_async_wait<kStages - 1>(); // this thread's Q copies have landed
+    __syncthreads();              // everyone's have
+    unsigned qf[D / 16][4];
+#pragma unroll
+    for (int kb = 0; kb < D / 16; ++kb)
+        ldsm_x4(qf[kb][0], qf[kb][1], qf[kb][2], qf[kb][3], qsm + swz<D>(lane & 15, kb * 2 + (lane >> 4)));
 
-    float acc[R][DPL];
+    // running state of rows lane / 4 and lane / 4 + 8 over this warp's keys (the mma.sync
+    // accumulator layout: o[db] holds columns 8 db + 2 (lane % 4) + {0, 1})
+    float o[D / 8][4];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int c = 0; c < DPL; ++c)
-            acc[r][c] = 0.f;
+    for (int db = 0; db < D / 8; ++db)
+        o[db][0] = o[db][1] = o[db][2] = o[db][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
     for (int t = 0; t < nt; ++t) {
         cp_async_wait<kStages - 2>(); // this thread's copies of tile t have landed
@@ -259,102 +250,133 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kern
                 load_tile(tn, tn % kStages);
             cp_async_commit();
         }
-        const T *ks = kv + (t % kStages) * L::kStageElems;
-        const T *vs = ks + kKT * L::kKs;
-        const int key0 = (t0 + t) * kKT;
+        const T *ks = kvs + (t % kStages) * (L::kStageBytes / 2);
+        const T *vs = ks + L::kTileBytes / 2;
+        const int key0 = (t0 + t) * kKT + warp * 16;
 
-        // scores: this lane's key, this warp's quarter of the head dimension, every row
-        {
-            float kf[DQ];
-            const T *krow = ks + lane * L::kKs + warp * DQ;
+        // S = Q K^T over this warp's 16 keys
+        float s[2][4];
 #pragma unroll
-            for (int c = 0; c < DQ / 8; ++c) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(krow + c * 8);
-                const float2 f0 = Elt<T>::pair(w.x), f1 = Elt<T>::pair(w.y);
-                const float2 f2 = Elt<T>::pair(w.z), f3 = Elt<T>::pair(w.w);
-                kf[c * 8 + 0] = f0.x; kf[c * 8 + 1] = f0.y; kf[c * 8 + 2] = f1.x; kf[c * 8 + 3] = f1.y;
-                kf[c * 8 + 4] = f2.x; kf[c * 8 + 5] = f2.y; kf[c * 8 + 6] = f3.x; kf[c * 8 + 7] = f3.y;
-            }
+        for (int nb = 0; nb < 2; ++nb)
+            s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float *qr = qs + r * D + warp * DQ;
-                float s0 = 0.f, s1 = 0.f;
+        for (int kb = 0; kb < D / 16; ++kb) {
+            unsigned b0, b1, b2, b3;
+            const int r = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int ch = kb * 2 + ((lane >> 3) & 1);
+            ldsm_x4(b0, b1, b2, b3, ks + swz<D>(r, ch));
+            Mma<T>::run(s[0], qf[kb], b0, b1);
+            Mma<T>::run(s[1], qf[kb], b2, b3);
+        }
+        // log2 units, row limits, running maximum
+        float mx[2] = {m[0], m[1]};
 #pragma unroll
-                for (int c = 0; c < DQ; c += 4) {
-                    const float4 q4 = *reinterpret_cast<const float4 *>(qr + c);
-                    s0 = fmaf(q4.x, kf[c], s0);
-                    s1 = fmaf(q4.y, kf[c + 1], s1);
-                    s0 = fmaf(q4.z, kf[c + 2], s0);
-                    s1 = fmaf(q4.w, kf[c + 3], s1);
-                }
-                sp[(warp * R + r) * kKT + lane] = s0 + s1;
+        for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float x = s[nb][e] * a.scale_log2;
+                const int key = key0 + nb * 8 + ((lane & 3) << 1) + (e & 1);
+                if (key >= (e < 2 ? lim_a : lim_b))
+                    x = -INFINITY;
+                s[nb][e] = x;
+                mx[e >> 1] = fmaxf(mx[e >> 1], x);
             }
         }
-        __syncthreads();
-
-        // softmax step of rows warp, warp + 4, ...: lane = key
+        float m_use[2], alpha[2];
 #pragma unroll
-        for (int r = warp; r < R; r += kWarps) {
-            float s = sp[(0 * R + r) * kKT + lane] + sp[(1 * R + r) * kKT + lane] +
-                      sp[(2 * R + r) * kKT + lane] + sp[(3 * R + r) * kKT + lane];
-            if (key0 + lane >= lim_s[r])
-                s = -INFINITY;
-            const float m_old = m_s[r];
-            const float l_old = l_s[r];
-            const float m_new = fmaxf(m_old, warp_max(s));
-            const float m_use = m_new == -INFINITY ? 0.f : m_new; // no key yet: P = 0
-            const float p = ex2(s - m_use);
-            const float sum = warp_sum(p);
-            pt[lane * R + r] = p;
-            __syncwarp();
-            if (lane == 0) {
-                const float alpha = ex2(m_old - m_use);
-                al_s[r] = alpha;
-                m_s[r] = m_new;
-                l_s[r] = l_old * alpha + sum;
-            }
+        for (int r = 0; r < 2; ++r) {
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+            m_use[r] = mx[r] == -INFINITY ? 0.f : mx[r]; // no key yet: P = 0, not NaN
+            alpha[r] = ex2(m[r] - m_use[r]);
+            m[r] = mx[r];
         }
-        __syncthreads();
-
-        // O = alpha * O + P V over this warp's keys; lane = columns lane * DPL ...
+        // P = 2^(S - m) as the A fragment of the second product; this thread's row sums
+        unsigned pf[4];
+        float rs[2] = {0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float al = al_s[r];
-#pragma unroll
-            for (int c = 0; c < DPL; ++c)
-                acc[r][c] *= al;
+        for (int nb = 0; nb < 2; ++nb) {
+            const float p0 = ex2(s[nb][0] - m_use[0]);
+            const float p1 = ex2(s[nb][1] - m_use[0]);
+            const float p2 = ex2(s[nb][2] - m_use[1]);
+            const float p3 = ex2(s[nb][3] - m_use[1]);
+            rs[0] += p0 + p1;
+            rs[1] += p2 + p3;
+            pf[2 * nb] = Mma<T>::pack(p0, p1);
+            pf[2 * nb + 1] = Mma<T>::pack(p2, p3);
         }
 #pragma unroll
-        for (int jj = 0; jj < KPW; ++jj) {
-            const int j = warp * KPW + jj;
-            float vf[DPL];
-            load_cols<T, DPL>(vf, vs + j * L::kVs + lane * DPL);
-            const float *pj = pt + j * R;
+        for (int r = 0; r < 2; ++r)
+            l[r] = l[r] * alpha[r] + rs[r];
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-            for (int r = 0; r < R; r += 4) {
-                const float4 p4 = *reinterpret_cast<const float4 *>(pj + r);
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) {
-                    acc[r][c] = fmaf(p4.x, vf[c], acc[r][c]);
-                    acc[r + 1][c] = fmaf(p4.y, vf[c], acc[r + 1][c]);
-                    acc[r + 2][c] = fmaf(p4.z, vf[c], acc[r + 2][c]);
-                    acc[r + 3][c] = fmaf(p4.w, vf[c], acc[r + 3][c]);
-                }
+            for (int db = 0; db < D / 8; ++db) {
+                o[db][0] *= alpha[0];
+                o[db][1] *= alpha[0];
+                o[db][2] *= alpha[1];
+                o[db][3] *= alpha[1];
             }
+        }
+        // O += P V over the same 16 keys
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            unsigned b0, b1, b2, b3;
+            const int r = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int ch = dp * 2 + (lane >> 4);
+            ldsm_x4_t(b0, b1, b2, b3, vs + swz<D>(r, ch));
+            Mma<T>::run(o[2 * dp], pf, b0, b1);
+            Mma<T>::run(o[2 * dp + 1], pf, b2, b3);
         }
     }
     cp_async_wait<0>();
-    __syncthreads(); // every stage read; the stages now hold the warps' partial outputs
+    __syncthreads(); // every stage read; the stages now hold the partial outputs
 
-    float *ob = reinterpret_cast<float *>(smem + L::kKv); // fp32 [kWarps][R][D]
+    // this warp's partial (m, l, O) of every row into shared memory
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < 2; ++r) {
+        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+    }
+    float *ow = reinterpret_cast<float *>(smem + L::kOw);
+    float *ob = reinterpret_cast<float *>(smem + L::kOb);
+    const int ra = lane >> 2, rb = ra + 8;
 #pragma unroll
-        for (int c = 0; c < DPL; ++c)
-            ob[(warp * R + r) * D + lane * DPL + c] = acc[r][c];
+    for (int db = 0; db < D / 8; ++db) {
+        const int col = db * 8 + ((lane & 3) << 1);
+        ow[(warp * kRows + ra) * D + col] = o[db][0];
+        ow[(warp * kRows + ra) * D + col + 1] = o[db][1];
+        ow[(warp * kRows + rb) * D + col] = o[db][2];
+        ow[(warp * kRows + rb) * D + col + 1] = o[db][3];
+    }
+    if ((lane & 3) == 0) {
+        mw[warp * kRows + ra] = m[0];
+        mw[warp * kRows + rb] = m[1];
+        lw[warp * kRows + ra] = l[0];
+        lw[warp * kRows + rb] = l[1];
+    }
     __syncthreads();
-    for (int e = tid; e < R * D; e += kThreads)
-        ob[e] = ob[e] + ob[R * D + e] + ob[2 * R * D + e] + ob[3 * R * D + e];
+    // the four warps merged into the CTA's partial
+    for (int e = tid; e < kRows * D; e += kThreads) {
+        const int r = e / D, col = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            M = fmaxf(M, mw[w * kRows + r]);
+        float os = 0.f, ls = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float wt = ex2(mw[w * kRows + r] - M);
+                os = fmaf(ow[(w * kRows + r) * D + col], wt, os);
+                ls = fmaf(lw[w * kRows + r], wt, ls);
+            }
+        }
+        ob[e] = os;
+        if (col == 0) {
+            m_s[r] = M;
+            l_s[r] = ls;
+        }
+    }
     __syncwarp();   // the cluster barrier is taken by whole warps
     cluster_sync(); // every CTA's (m, l, O) is complete and visible to the cluster
 
@@ -379,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kern
             out = Osum / Lsum;
             lse = (M + log2f(Lsum)) * kLn2;
         }
-        og[e] = Elt<T>::from(out);
+        og[e] = Mma<T>::from(out);
         if (col == 0 && a.lse)
             a.lse[bh * a.N + r] = lse;
     }
@@ -391,14 +413,14 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 4 : 3) attn_fwd_decode_kern
 // cluster size that the device can place is known (0: not looked up yet).
 constexpr int kMaxDevices = 64;
 std::mutex g_cfg_mutex;
-int g_cfg_cmax[kMaxDevices][3][3][2];
-int g_cfg_per_sm[kMaxDevices][3][3][2];
+int g_cfg_cmax[kMaxDevices][3][2];
+int g_cfg_per_sm[kMaxDevices][3][2];
 
-template <int D, int R, typename T>
+template <int D, typename T>
 cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream)
 {
-    auto kernel = attn_fwd_decode_kernel<D, R, T>;
-    constexpr int smem = DecSmem<D, R>::kBytes;
+    auto kernel = attn_fwd_decode_kernel<D, T>;
+    constexpr int smem = DecSmem<D>::kBytes;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -406,13 +428,12 @@ cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream)
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     const int di = D == 32 ? 0 : D == 64 ? 1 : 2;
-    const int ri = R == 4 ? 0 : R == 8 ? 1 : 2;
     const int ti = std::is_same<T, __half>::value ? 0 : 1;
     int cmax, per_sm;
     {
         std::lock_guard<std::mutex> lock(g_cfg_mutex);
-        cmax = g_cfg_cmax[dev][di][ri][ti];
-        per_sm = g_cfg_per_sm[dev][di][ri][ti];
+        cmax = g_cfg_cmax[dev][di][ti];
+        per_sm = g_cfg_per_sm[dev][di][ti];
         if (cmax == 0) {
             err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (err != cudaSuccess)
@@ -441,8 +462,8 @@ cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream)
                     break;
                 (void)cudaGetLastError(); // a refused size leaves no error behind
             }
-            g_cfg_cmax[dev][di][ri][ti] = cmax;
-            g_cfg_per_sm[dev][di][ri][ti] = per_sm;
+            g_cfg_cmax[dev][di][ti] = cmax;
+            g_cfg_per_sm[dev][di][ti] = per_sm;
         }
     }
     int sms = 0;
@@ -488,21 +509,12 @@ cudaError_t launch_cfg(const FwdParams &p, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
-template <int D, typename T> cudaError_t launch_rows(const FwdParams &p, cudaStream_t stream)
-{
-    if (p.N <= 4)
-        return launch_cfg<D, 4, T>(p, stream);
-    if (p.N <= 8)
-        return launch_cfg<D, 8, T>(p, stream);
-    return launch_cfg<D, 16, T>(p, stream);
-}
-
 template <typename T> cudaError_t launch_dtype(const FwdParams &p, cudaStream_t stream)
 {
     switch (p.d) {
-    case 32: return launch_rows<32, T>(p, stream);
-    case 64: return launch_rows<64, T>(p, stream);
-    case 128: return launch_rows<128, T>(p, stream);
+    case 32: return launch_cfg<32, T>(p, stream);
+    case 64: return launch_cfg<64, T>(p, stream);
+    case 128: return launch_cfg<128, T>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
