@@ -96,8 +96,9 @@ typedef enum {
 
 /* Which kernel runs the forward. AUTO runs the decoding kernel for problems of at most 16
  * query rows per head (after the query-group packing of attn_fwd_ex) over at least
- * ATTN_DECODE_MIN_KEYS keys in fp16 or bf16, the short-sequence kernel for d = 32 with
- * N <= 256, and the tiled tcgen05 kernel everywhere else (the fastest at every measured
+ * ATTN_DECODE_MIN_KEYS keys in fp16 or bf16, the short-sequence kernel for fp16
+ * self-attention with d = 32 and N <= 256, the warp-level split-TF32 kernel for fp32 inputs
+ * (fp32 accuracy), and the tiled tcgen05 kernel everywhere else (the fastest at every measured
  * shape); the other kernels remain selectable explicitly. */
 typedef enum {
     ATTN_PATH_AUTO = 0,
