@@ -136,8 +136,8 @@ attn_status_t attn_fwd_lse(const void *q, const void *k, const void *v, void *o,
                            const int32_t *key_lengths, attn_stream_t stream);
 
 /* attn_fwd_lse with an explicit kernel choice (attn_path_t). A kernel asked for a
- * shape it does not take (ATTN_PATH_SHORT with N > 256 or d = 128) returns
- * ATTN_ERR_UNSUPPORTED. Used to check each kernel on every shape it serves. */
+ * shape it does not take (ATTN_PATH_SHORT with N > 256 or d = 128, ATTN_PATH_DECODE with
+ * N > 16) returns ATTN_ERR_UNSUPPORTED. Used to check each kernel on every shape it serves. */
 attn_status_t attn_fwd_path(const void *q, const void *k, const void *v, void *o, float *lse,
                             int B, int H, int N, int d, float sm_scale, int causal,
                             const int32_t *key_lengths, int path, attn_stream_t stream);
