@@ -235,3 +235,26 @@ def test_splitkv_ex_validation(lib):
     assert lib.attn_splitkv_auto_splits_ex(1, 4, 2, 8, 32, 48, 0) == -1
     assert lib.attn_splitkv_auto_splits_ex(1, 4, 2, 8, 32, 64, 2) == -1
     assert lib.attn_splitkv_auto_splits_ex(1, 4, 3, 8, 32, 64, 0) == -1  # H not a multiple of H_kv
+
+
+@pytest.mark.parametrize("args,expected", [
+    # H, H_kv, N_q, N_k, d, dtype, causal -> kernel
+    ((32, 8, 1, 8192, 128, _lib.DTYPE_F16, 1), _lib.PATH_DECODE),    # 4 packed rows
+    ((32, 8, 4, 8192, 128, _lib.DTYPE_BF16, 1), _lib.PATH_DECODE),   # 16 packed rows
+    ((32, 8, 5, 8192, 128, _lib.DTYPE_F16, 1), _lib.PATH_TCGEN05),   # 20 packed rows
+    ((32, 8, 1, 256, 64, _lib.DTYPE_F16, 0), _lib.PATH_DECODE),      # the fewest keys it takes
+    ((32, 8, 1, 255, 64, _lib.DTYPE_F16, 0), _lib.PATH_TCGEN05),
+    ((4, 4, 16, 4096, 32, _lib.DTYPE_F16, 0), _lib.PATH_DECODE),     # unpacked, 16 rows
+    ((4, 4, 17, 4096, 32, _lib.DTYPE_F16, 0), _lib.PATH_TCGEN05),
+    ((32, 8, 1, 8192, 32, _lib.DTYPE_F32, 1), _lib.PATH_WARP_MMA),   # fp32: fp32 accuracy
+    ((12, 12, 256, 256, 32, _lib.DTYPE_F16, 0), _lib.PATH_SHORT),    # self-attention, short
+    ((32, 32, 4096, 4096, 128, _lib.DTYPE_F16, 1), _lib.PATH_TCGEN05),
+    ((32, 32, 4096, 4096, 128, _lib.DTYPE_BF16, 1), _lib.PATH_TCGEN05),
+    ((4, 3, 1, 512, 64, _lib.DTYPE_F16, 0), -1),                     # H not a multiple of H_kv
+    ((4, 4, 1, 512, 48, _lib.DTYPE_F16, 0), -1),
+    ((4, 4, 1, 512, 64, _lib.DTYPE_F32, 0), -1),                     # fp32 needs d = 32
+    ((4, 4, 1, 512, 64, _lib.DTYPE_F16, 2), -1),
+])
+def test_auto_path_ex(lib, args, expected):
+    """The automatic kernel choice of attn_fwd_ex, a host computation (no device needed)."""
+    assert lib.attn_auto_path_ex(*args) == expected
